@@ -1,0 +1,349 @@
+/*
+ * ORACLE -- test infrastructure, not part of the product.
+ *
+ * A plain, slow, single-threaded C definition of the routed MoE FFN layer,
+ * used only by the test suite, by the package's smoke check and by the CPU
+ * baseline leg of the benchmark.  It shares no code with the CUDA library and
+ * includes none of its headers.
+ *
+ * What the layer is, and where it is stated:
+ *  - thewafflehaus/butter PR #69, commit "feat(laguna): Laguna-S-2.1 decode on
+ *    the CUDA engine": the MoE layer is a sigmoid top-10 router with
+ *    score-correction bias and a shared expert; expert weights are Q4
+ *    (re-quantised at load); gate and up are fused (SwiGLU).
+ *  - same page, commit "feat(laguna): batched prefill with tensor-core
+ *    projections, fused MoE, CTA scheduling": grouped-GEMM MoE with on-device
+ *    descriptors (per-expert counts, offsets and a token order), fused gate+up
+ *    expert stacks, a W4A16 shared expert.
+ *  - thewafflehaus/FFAI PR #72, Nemotron W4A16 Marlin MoE commit: CSR offsets
+ *    [n_exp+1], router-sorted token indices, deterministic scatter-add.
+ *  - the layer statement accompanying the pages fixes the rest: the bias is
+ *    used for selection only; combine weights are the selected sigmoid scores
+ *    normalised to sum 1; int4 symmetric per group along K with
+ *    scale = absmax/7 stored as fp16 and q = clamp(round(w/s), -8, 7), two
+ *    nibbles per byte; activations bf16, fp32 accumulation, bf16 output.
+ *
+ * Readings taken where the statement is open (each is listed with its reason
+ * in the design notes):
+ *  R1 dequantised weight w^ = q * s exactly (fp32 holds it exactly: 4 x 11
+ *     significant bits); no intermediate rounding of w^.
+ *  R2 round(.) is round-half-to-even (rint); s is absmax/7 in fp32, then
+ *     rounded to fp16; an all-zero group has s = 0 and q = 0.
+ *  R3 nibble order: byte j of a row holds element 2j in bits 0-3 and element
+ *     2j+1 in bits 4-7, each as 4-bit two's complement.
+ *  R4 SwiGLU: h = silu(gate) * up with gate rows 0..F-1 and up rows F..2F-1 of
+ *     the fused gate+up matrix; silu(z) = z / (1 + e^-z).
+ *  R5 rounding points: x (bf16 input), h (bf16), out (bf16).  Router logits
+ *     and scores in fp64; expert dot products accumulate in fp32 in ascending
+ *     index order; the combine accumulates in fp32 in the order
+ *     j = 0..k-1 then the shared expert.
+ *  R6 selection: the k largest s + b, ties to the lower expert id, listed in
+ *     descending order; combine weights w_j = s_j / sum_j s_j.
+ *  R7 shared expert: weight 1, no gate.
+ *  R8 descriptors: perm lists slot ids t*k + j sorted by (expert, token);
+ *     pos is its inverse; sched orders experts by count, largest first, ties
+ *     to the lower id.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* Number formats (IEEE 754 binary16 and bfloat16), from their definitions. */
+
+typedef struct {
+    int p;        /* significant bits, including the implicit one */
+    int emin;     /* exponent of the smallest normal */
+    int emax;     /* exponent of the largest finite binade */
+    int bias;
+} orc_fmt;
+
+static const orc_fmt FMT_F16 = {11, -14, 15, 15};
+static const orc_fmt FMT_BF16 = {8, -126, 127, 127};
+
+/* Round a >= 0 (finite) to the nearest value of format f, ties to even.
+   Returns +INFINITY on overflow. */
+static double round_to_fmt(double a, orc_fmt f) {
+    if (a == 0.0) return 0.0;
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1; /* a in [2^e, 2^(e+1)) */
+    if (e < f.emin) e = f.emin;
+    double quantum = ldexp(1.0, e - (f.p - 1));
+    double r = rint(a / quantum) * quantum;
+    double maxfin = ldexp(2.0 - ldexp(1.0, 1 - f.p), f.emax);
+    if (r > maxfin) return INFINITY;
+    return r;
+}
+
+static uint16_t encode_fmt(double v, int neg, orc_fmt f) {
+    int fbits = f.p - 1;
+    uint16_t sign = neg ? (uint16_t)0x8000 : 0;
+    if (isnan(v)) return (uint16_t)(sign | (((1u << (15 - fbits)) - 1) << fbits) | (1u << (fbits - 1)));
+    if (v == 0.0) return sign;
+    if (isinf(v)) return (uint16_t)(sign | (((1u << (15 - fbits)) - 1) << fbits));
+    int ex;
+    frexp(v, &ex);
+    int e = ex - 1;
+    if (e < f.emin) {
+        double frac = v / ldexp(1.0, f.emin - fbits); /* subnormal: integer < 2^fbits */
+        return (uint16_t)(sign | (uint16_t)frac);
+    }
+    double frac = (v / ldexp(1.0, e) - 1.0) * ldexp(1.0, fbits);
+    return (uint16_t)(sign | ((uint16_t)(e + f.bias) << fbits) | (uint16_t)frac);
+}
+
+static double decode_fmt(uint16_t h, orc_fmt f) {
+    int fbits = f.p - 1;
+    int ebits = 15 - fbits;
+    int neg = (h >> 15) & 1;
+    unsigned ef = (h >> fbits) & ((1u << ebits) - 1);
+    unsigned frac = h & ((1u << fbits) - 1);
+    double v;
+    if (ef == (1u << ebits) - 1) v = frac ? NAN : INFINITY;
+    else if (ef == 0) v = (double)frac * ldexp(1.0, f.emin - fbits);
+    else v = (1.0 + (double)frac * ldexp(1.0, -fbits)) * ldexp(1.0, (int)ef - f.bias);
+    return neg ? -v : v;
+}
+
+static uint16_t to_fmt(double x, orc_fmt f) {
+    if (isnan(x)) return encode_fmt(x, 0, f);
+    int neg = signbit(x) ? 1 : 0;
+    return encode_fmt(round_to_fmt(fabs(x), f), neg, f);
+}
+
+uint16_t orc_f32_to_f16(float x) { return to_fmt((double)x, FMT_F16); }
+float orc_f16_to_f32(uint16_t h) { return (float)decode_fmt(h, FMT_F16); }
+uint16_t orc_f32_to_bf16(float x) { return to_fmt((double)x, FMT_BF16); }
+uint16_t orc_f64_to_bf16(double x) { return to_fmt(x, FMT_BF16); }
+float orc_bf16_to_f32(uint16_t h) { return (float)decode_fmt(h, FMT_BF16); }
+
+/* ------------------------------------------------------------------ */
+/* int4 weights: quantise / pack, and the exact dequantised value.      */
+
+static int nibble_value(const uint8_t* q_row, int64_t i) {
+    unsigned byte = q_row[i / 2];
+    unsigned nib = (i % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
+    return (nib >= 8) ? (int)nib - 16 : (int)nib; /* 4-bit two's complement */
+}
+
+void orc_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group, uint8_t* q,
+                 uint16_t* s) {
+    int64_t ngroups = K / group;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* wr = w + r * K;
+        uint8_t* qr = q + r * (K / 2);
+        memset(qr, 0, (size_t)(K / 2));
+        for (int64_t gi = 0; gi < ngroups; ++gi) {
+            float absmax = 0.0f;
+            for (int64_t i = gi * group; i < (gi + 1) * group; ++i) {
+                float a = fabsf(wr[i]);
+                if (a > absmax) absmax = a;
+            }
+            uint16_t s16 = orc_f32_to_f16(absmax / 7.0f);
+            s[r * ngroups + gi] = s16;
+            float sf = orc_f16_to_f32(s16);
+            for (int64_t i = gi * group; i < (gi + 1) * group; ++i) {
+                int qi = 0;
+                if (sf != 0.0f) {
+                    float t = wr[i] / sf;
+                    float rt = rintf(t);
+                    if (rt < -8.0f) rt = -8.0f;
+                    if (rt > 7.0f) rt = 7.0f;
+                    qi = (int)rt;
+                }
+                unsigned nib = (unsigned)qi & 0xFu;
+                qr[i / 2] |= (uint8_t)((i % 2 == 0) ? nib : (nib << 4));
+            }
+        }
+    }
+}
+
+void orc_dequant_w4(const uint8_t* q, const uint16_t* s, int64_t rows, int64_t K, int32_t group,
+                    float* w_hat) {
+    int64_t ngroups = K / group;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t i = 0; i < K; ++i)
+            w_hat[r * K + i] = (float)nibble_value(q + r * (K / 2), i) *
+                               orc_f16_to_f32(s[r * ngroups + i / group]);
+}
+
+/* ------------------------------------------------------------------ */
+/* Router: fp64 logits and sigmoid scores, biased top-k selection.      */
+
+void orc_router(const uint16_t* x, const float* W_r, const float* bias, int64_t T, int32_t d,
+                int32_t E, int32_t k, int64_t t0, int64_t t1, int32_t* topk_idx, float* topk_w,
+                double* margin, double* scores) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)E);
+    double* key = (double*)malloc(sizeof(double) * (size_t)E);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    (void)T;
+    for (int64_t t = t0; t < t1; ++t) {
+        const uint16_t* xt = x + t * d;
+        for (int32_t e = 0; e < E; ++e) {
+            double l = 0.0;
+            for (int32_t i = 0; i < d; ++i)
+                l += (double)orc_bf16_to_f32(xt[i]) * (double)W_r[(int64_t)e * d + i];
+            s[e] = 1.0 / (1.0 + exp(-l));
+            key[e] = s[e] + (double)bias[e];
+            taken[e] = 0;
+            if (scores) scores[t * E + e] = s[e];
+        }
+        double kth = 0.0;
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t best = -1;
+            for (int32_t e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || key[e] > key[best])) best = e;
+            taken[best] = 1;
+            topk_idx[t * k + j] = best;
+            kth = key[best];
+        }
+        if (margin) {
+            if (k < E) {
+                int32_t next = -1;
+                for (int32_t e = 0; e < E; ++e)
+                    if (!taken[e] && (next < 0 || key[e] > key[next])) next = e;
+                margin[t] = kth - key[next];
+            } else {
+                margin[t] = INFINITY;
+            }
+        }
+        double sum = 0.0;
+        for (int32_t j = 0; j < k; ++j) sum += s[topk_idx[t * k + j]];
+        for (int32_t j = 0; j < k; ++j)
+            topk_w[t * k + j] = (float)(s[topk_idx[t * k + j]] / sum);
+    }
+    free(s);
+    free(key);
+    free(taken);
+}
+
+/* ------------------------------------------------------------------ */
+/* Expert descriptors.                                                  */
+
+void orc_descriptors(const int32_t* topk_idx, int64_t T, int32_t E, int32_t k, int32_t* counts,
+                     int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched) {
+    if (E <= 0) return;
+    for (int32_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t sl = 0; sl < T * k; ++sl) counts[topk_idx[sl]] += 1;
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int64_t cursor = 0;
+    for (int32_t e = 0; e < E; ++e)
+        for (int64_t t = 0; t < T; ++t)
+            for (int32_t j = 0; j < k; ++j)
+                if (topk_idx[t * k + j] == e) perm[cursor++] = (int32_t)(t * k + j);
+    for (int64_t r = 0; r < T * k; ++r) pos[perm[r]] = (int32_t)r;
+    /* experts by count, largest first; equal counts keep ascending ids */
+    unsigned char* used = (unsigned char*)calloc((size_t)E, 1);
+    for (int32_t i = 0; i < E; ++i) {
+        int32_t best = -1;
+        for (int32_t e = 0; e < E; ++e)
+            if (!used[e] && (best < 0 || counts[e] > counts[best])) best = e;
+        used[best] = 1;
+        sched[i] = best;
+    }
+    free(used);
+}
+
+/* ------------------------------------------------------------------ */
+/* One expert on one token: fused gate+up SwiGLU, then the down projection. */
+
+static float dot_w4_row(const float* xf, const uint8_t* q_row, const uint16_t* s_row, int64_t K,
+                        int32_t group) {
+    float acc = 0.0f;
+    for (int64_t gi = 0; gi < K / group; ++gi) {
+        float sc = orc_f16_to_f32(s_row[gi]);
+        for (int64_t i = gi * group; i < (gi + 1) * group; ++i) {
+            float w_hat = (float)nibble_value(q_row, i) * sc; /* exact */
+            acc += xf[i] * w_hat;                             /* product exact; sum rounds */
+        }
+    }
+    return acc;
+}
+
+void orc_expert_token(const uint16_t* x, int32_t d, int32_t F, int32_t group,
+                      const uint8_t* q_gu, const uint16_t* s_gu, const uint8_t* q_dn,
+                      const uint16_t* s_dn, uint16_t* h, float* y) {
+    float* xf = (float*)malloc(sizeof(float) * (size_t)d);
+    float* hf = (float*)malloc(sizeof(float) * (size_t)F);
+    for (int32_t i = 0; i < d; ++i) xf[i] = orc_bf16_to_f32(x[i]);
+    int64_t gu_row_bytes = d / 2, gu_row_scales = d / group;
+    for (int32_t f = 0; f < F; ++f) {
+        float g = dot_w4_row(xf, q_gu + (int64_t)f * gu_row_bytes, s_gu + (int64_t)f * gu_row_scales,
+                             d, group);
+        float u = dot_w4_row(xf, q_gu + (int64_t)(F + f) * gu_row_bytes,
+                             s_gu + (int64_t)(F + f) * gu_row_scales, d, group);
+        double silu = (double)g / (1.0 + exp(-(double)g));
+        h[f] = orc_f64_to_bf16(silu * (double)u);
+        hf[f] = orc_bf16_to_f32(h[f]);
+    }
+    int64_t dn_row_bytes = F / 2, dn_row_scales = F / group;
+    for (int32_t c = 0; c < d; ++c)
+        y[c] = dot_w4_row(hf, q_dn + (int64_t)c * dn_row_bytes, s_dn + (int64_t)c * dn_row_scales, F,
+                          group);
+    free(xf);
+    free(hf);
+}
+
+/* ------------------------------------------------------------------ */
+/* The layer for a list of tokens, given the selection.                 */
+
+void orc_layer_tokens(const uint16_t* x, int32_t d, int32_t E, int32_t k, int32_t F, int32_t Fs,
+                      int32_t group, const int32_t* topk_idx, const float* topk_w,
+                      const uint8_t* q_gu, const uint16_t* s_gu, const uint8_t* q_dn,
+                      const uint16_t* s_dn, const uint8_t* qs_gu, const uint16_t* ss_gu,
+                      const uint8_t* qs_dn, const uint16_t* ss_dn, const int64_t* tokens,
+                      int64_t n_tokens, uint16_t* out, uint16_t* h_routed, uint16_t* h_shared) {
+    int64_t gu_bytes = (int64_t)2 * F * (d / 2), gu_scales = (int64_t)2 * F * (d / group);
+    int64_t dn_bytes = (int64_t)d * (F / 2), dn_scales = (int64_t)d * (F / group);
+    float* y = (float*)malloc(sizeof(float) * (size_t)d);
+    float* acc = (float*)malloc(sizeof(float) * (size_t)d);
+    uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(F > Fs ? F : Fs));
+    (void)E;
+    for (int64_t n = 0; n < n_tokens; ++n) {
+        int64_t t = tokens[n];
+        const uint16_t* xt = x + t * d;
+        for (int32_t c = 0; c < d; ++c) acc[c] = 0.0f;
+        for (int32_t j = 0; j < k; ++j) {
+            int64_t e = topk_idx[t * k + j];
+            float wj = topk_w[t * k + j];
+            orc_expert_token(xt, d, F, group, q_gu + e * gu_bytes, s_gu + e * gu_scales,
+                             q_dn + e * dn_bytes, s_dn + e * dn_scales, h, y);
+            if (h_routed) memcpy(h_routed + (n * k + j) * F, h, sizeof(uint16_t) * (size_t)F);
+            for (int32_t c = 0; c < d; ++c) {
+                float p = wj * y[c];
+                acc[c] = acc[c] + p;
+            }
+        }
+        orc_expert_token(xt, d, Fs, group, qs_gu, ss_gu, qs_dn, ss_dn, h, y);
+        if (h_shared) memcpy(h_shared + n * Fs, h, sizeof(uint16_t) * (size_t)Fs);
+        for (int32_t c = 0; c < d; ++c) {
+            acc[c] = acc[c] + y[c];
+            out[n * d + c] = orc_f32_to_bf16(acc[c]);
+        }
+    }
+    free(y);
+    free(acc);
+    free(h);
+}
+
+/* ------------------------------------------------------------------ */
+/* Element-wise helpers over arrays (used by the tests' format pins).   */
+
+void orc_f32_to_f16_array(const float* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_f16(x[i]);
+}
+void orc_f16_to_f32_array(const uint16_t* h, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_to_f32(h[i]);
+}
+void orc_f32_to_bf16_array(const float* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(x[i]);
+}
+void orc_f64_to_bf16_array(const double* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f64_to_bf16(x[i]);
+}
+void orc_bf16_to_f32_array(const uint16_t* h, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_to_f32(h[i]);
+}
