@@ -1,0 +1,497 @@
+"""Benchmark of the routed MoE FFN layer on GB300.
+
+One step = one pass of the whole layer (router, descriptors, fused gate+up
+SwiGLU, down projection, combine with the shared expert) over one batch of
+synthetic tokens, through the C ABI (moe_layer_forward), replayed as a CUDA
+graph.  The headline workload is single-token decode (T = 1, d 4096, 256
+experts, top-10, FFN 1024 + shared 1024, int4 g128); the same JSON line also
+carries the T = 2048 chunked-prefill pass under "secondary".
+
+Inputs larger than L2: each step reads a different copy of the packed
+weights (NCOPY copies, each 1.67 GB) and a different activation batch, so
+no step finds its weights in the 129 MB L2.
+
+--impl reference times the CPU oracle (the plain C definition of the layer)
+on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+HEADLINE = "decode1"
+SECONDARY = "prefill2048"
+METRIC = "MoE-layer tokens/s at T=1 and T=2048; % of HBM / BF16 tensor-core roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def kernels_per_step(cfg, flags=0):
+    """Kernels libmoe.so launches for one moe_layer_forward (memset nodes excluded)."""
+    router = 2
+    desc = 2
+    experts = 2
+    combine = 1
+    return router + desc + experts + combine
+
+
+class GpuBench:
+    def __init__(self, cfg, device, ncopy: int, nbatch: int):
+        import torch
+
+        import moe_expert_layer_sigmoid_gb300 as moe
+        from workloads.device import upload
+
+        self.torch, self.moe = torch, moe
+        self.cfg = cfg
+        self.device = device
+        self.layer = upload(cfg, device=device, extra_batches=nbatch - 1)
+        L = self.layer
+        self.xs = [L.x] + list(L.x_batches)
+        # weight copies: copy 0 is the uploaded one
+        self.copies = [L.w4s()]
+        self._keep = []
+        for _ in range(ncopy - 1):
+            ts = [t.clone() for t in (L.gu_q, L.gu_s, L.dn_q, L.dn_s, L.sgu_q, L.sgu_s, L.sdn_q,
+                                      L.sdn_s)]
+            self._keep.append(ts)
+            self.copies.append((moe.w4(ts[0], ts[1]), moe.w4(ts[2], ts[3]), moe.w4(ts[4], ts[5]),
+                                moe.w4(ts[6], ts[7])))
+        self.dims = L.dims()
+        self.ws = moe.workspace(moe.moe_layer_workspace_bytes(self.dims), device)
+        self.out = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=device)
+        self.stream = torch.cuda.Stream(device)
+        self.nslots = max(len(self.copies), len(self.xs))
+
+    def step(self, i, stream=None):
+        c = self.copies[i % len(self.copies)]
+        x = self.xs[i % len(self.xs)]
+        self.moe.moe_layer_forward(x, self.layer.W_r, self.layer.bias, self.dims, *c, self.out,
+                                   self.ws, stream=stream)
+
+    def capture(self):
+        torch = self.torch
+        self.graphs = []
+        with torch.cuda.stream(self.stream):
+            for i in range(self.nslots):  # warm every slot once outside capture
+                self.step(i, self.stream)
+        self.stream.synchronize()
+        for i in range(self.nslots):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.step(i, self.stream)
+            self.graphs.append(g)
+        torch.cuda.synchronize(self.device)
+
+    def run(self, warmup: int, steps: int):
+        torch = self.torch
+        for i in range(warmup):
+            self.graphs[i % self.nslots].replay()
+        torch.cuda.synchronize(self.device)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            start.record(self.stream)
+            for i in range(steps):
+                self.graphs[i % self.nslots].replay()
+            end.record(self.stream)
+        end.synchronize()
+        return start.elapsed_time(end) / steps  # ms per step
+
+    def descriptors(self, i):
+        """Per-slot counts (read back outside any timed region)."""
+        moe, torch = self.moe, self.torch
+        T, k, E = self.cfg.T, self.cfg.k, self.cfg.E
+        dims = self.dims
+        ws = moe.workspace(moe.moe_workspace_bytes(dims), self.device)
+        i32 = dict(dtype=torch.int32, device=self.device)
+        idx = torch.empty((T, k), **i32)
+        w = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+        perm, pos, sched = torch.empty(T * k, **i32), torch.empty(T * k, **i32), torch.empty(E, **i32)
+        moe.moe_router_topk(self.xs[i % len(self.xs)], self.layer.W_r, self.layer.bias, dims, idx, w,
+                            None, ws)
+        moe.moe_build_descriptors(idx, dims, counts, offsets, perm, pos, sched, ws)
+        torch.cuda.synchronize(self.device)
+        return dict(idx=idx, w=w, counts=counts, offsets=offsets, perm=perm, pos=pos, sched=sched,
+                    ws=ws)
+
+    def time_gateup(self, warmup: int, steps: int):
+        """Average duration of the gate+up kernel (the largest byte mover) per launch,
+        CUDA events on its own stream, rotating weight copies and batches."""
+        moe, torch = self.moe, self.torch
+        descs = [self.descriptors(i) for i in range(self.nslots)]
+        Fmax = max(self.cfg.F, self.cfg.Fs)
+        H = torch.empty((self.cfg.rows, Fmax), dtype=torch.int16, device=self.device)
+
+        def launch(i):
+            dsc = descs[i % self.nslots]
+            c = self.copies[i % len(self.copies)]
+            moe.moe_gateup_swiglu_w4a16(self.xs[i % len(self.xs)], self.dims, dsc["offsets"],
+                                        dsc["perm"], dsc["sched"], c[0], c[2], H, dsc["ws"],
+                                        stream=self.stream)
+
+        with torch.cuda.stream(self.stream):
+            for i in range(warmup):
+                launch(i)
+            self.stream.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(self.stream)
+            for i in range(steps):
+                launch(i)
+            end.record(self.stream)
+        end.synchronize()
+        active = [int((d["counts"] > 0).sum().item()) for d in descs]
+        return start.elapsed_time(end) / steps, active
+
+    def e2e(self, warmup: int, steps: int):
+        """moe_layer_forward_host: pinned host x in, pinned host out, captured as a graph."""
+        moe, torch = self.moe, self.torch
+        T, d = self.cfg.T, self.cfg.d
+        xh = [torch.empty((T, d), dtype=torch.int16, pin_memory=True) for _ in self.xs]
+        for a, b in zip(xh, self.xs):
+            a.copy_(b.cpu())
+        oh = torch.empty((T, d), dtype=torch.int16, pin_memory=True)
+        graphs = []
+        for i in range(self.nslots):
+            c = self.copies[i % len(self.copies)]
+            with torch.cuda.stream(self.stream):
+                moe.moe_layer_forward_host(xh[i % len(xh)], self.layer.W_r, self.layer.bias,
+                                           self.dims, *c, oh, self.ws, stream=self.stream)
+            self.stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                moe.moe_layer_forward_host(xh[i % len(xh)], self.layer.W_r, self.layer.bias,
+                                           self.dims, *c, oh, self.ws, stream=self.stream)
+            graphs.append(g)
+        for i in range(warmup):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize(self.device)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            start.record(self.stream)
+            for i in range(steps):
+                graphs[i % len(graphs)].replay()
+            end.record(self.stream)
+        end.synchronize()
+        ms = start.elapsed_time(end) / steps
+        return ms, 2 * T * d, 2 * T * d
+
+    def free(self):
+        self.graphs = []
+        self._keep = []
+        self.copies = []
+        self.layer = None
+        self.torch.cuda.empty_cache()
+
+
+def gpu_roofline_decode(cfg, gu_ms, active, pk, pk_kind):
+    """Gate+up kernel at decode: algorithmic bytes = packed gate+up bytes (+ scales) of the
+    active routed experts and the shared expert, per launch."""
+    per_expert = 2 * cfg.F * cfg.d // 2 + 2 * cfg.F * (cfg.d // cfg.group) * 2
+    shared = 2 * cfg.Fs * cfg.d // 2 + 2 * cfg.Fs * (cfg.d // cfg.group) * 2
+    nbytes = float(np.mean([a * per_expert + shared for a in active]))
+    achieved = nbytes / (gu_ms * 1e-3) / 1e9
+    peak = pk["hbm_gbs"]
+    return {"kernel": "gateup_gemv_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": None, "bytes_per_launch": int(nbytes), "launch_us": round(gu_ms * 1e3, 3),
+            "peak_source": f"{pk_kind} hbm_gbs"}
+
+
+def gpu_roofline_prefill(cfg, gu_ms, pk, pk_kind):
+    """Gate+up kernel at prefill: algorithmic flops = 2 * (2F) * d per routed slot and per
+    shared row."""
+    flops = 2.0 * 2 * cfg.d * (cfg.F * cfg.slots + cfg.Fs * cfg.T)
+    achieved = flops / (gu_ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops"]
+    return {"kernel": "gateup", "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+            "flops_per_launch": flops, "launch_us": round(gu_ms * 1e3, 2),
+            "peak_source": f"{pk_kind} bf16_tflops"}
+
+
+def measure_config(name, device, warmup, steps, ncopy, nbatch, pk, pk_kind, gpu_index):
+    cfg = workloads.CONFIGS[name]
+    b = GpuBench(cfg, device, ncopy=ncopy, nbatch=nbatch)
+    b.capture()
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    ms = b.run(warmup, steps)
+    clk = clocks.stop()
+    gu_ms, active = b.time_gateup(warmup, steps)
+    e2e_ms, h2d, d2h = b.e2e(warmup, steps)
+    layer_bytes = float(np.mean([(a + 1) * cfg.packed_expert_bytes() for a in active]))
+    res = dict(cfg=cfg, ms=ms, clocks=clk, gu_ms=gu_ms, active=active, e2e_ms=e2e_ms, h2d=h2d,
+               d2h=d2h, layer_bytes=layer_bytes, packed_copies=len(b.copies),
+               batches=len(b.xs))
+    b.free()
+    return res
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(cfg, budget_s: float, max_tokens: int):
+    """Time the oracle (router + experts + combine) on tokens of the workload until about
+    budget_s of CPU work; experts are quantised beforehand (load time, untimed).
+    Returns (tokens, seconds)."""
+    import oracle
+    done, spent, batch = 0, 0.0, 0
+    wr, bias = workloads.gen_router(cfg)
+    cache = {}
+
+    def packed(e):
+        if e not in cache:
+            cache[e] = (oracle.pack_w4(workloads.gen_gateup(cfg, e), cfg.group),
+                        oracle.pack_w4(workloads.gen_down(cfg, e), cfg.group))
+        return cache[e]
+
+    sq_gu, sq_dn = packed(-1)
+    while spent < budget_s and done < max_tokens:
+        x = workloads.gen_x(cfg, batch)[:1]
+        idx, w, _, _ = oracle.router(x, wr, bias, cfg.k)
+        sel = idx[0]
+        for e in sel:
+            packed(int(e))
+        # a compact expert stack holding only the selected experts (relabelled 0..k-1)
+        W = oracle.PackedLayer(
+            np.stack([cache[int(e)][0][0] for e in sel]), np.stack([cache[int(e)][0][1] for e in sel]),
+            np.stack([cache[int(e)][1][0] for e in sel]), np.stack([cache[int(e)][1][1] for e in sel]),
+            sq_gu[0], sq_gu[1], sq_dn[0], sq_dn[1], cfg.group)
+        local_idx = np.arange(cfg.k, dtype=np.int32)[None, :]
+        t0 = time.perf_counter()
+        oracle.router(x, wr, bias, cfg.k)
+        oracle.layer_tokens(x, W, local_idx, w, np.array([0]))
+        spent += time.perf_counter() - t0
+        done += 1
+        batch += 1
+    return done, spent
+
+
+# ---------------------------------------------------------------- main
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = workloads.CONFIGS[args.config]
+    # warm-up steps: one oracle token each, untimed
+    oracle_sample(cfg, budget_s=0.0, max_tokens=max(0, min(args.warmup, 1)))
+    n, sec = oracle_sample(cfg, budget_s=1e9, max_tokens=args.steps)
+    tps = n / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(tps, 4), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec / n * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (fp64 router)", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, top-{cfg.k}, "
+                               f"F={cfg.F}, shared F={cfg.Fs}, int4 g{cfg.group}",
+                   "step": "one token of the workload through the oracle"},
+        "cpu_baseline": {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} tokens of {cfg.name}, one per step, single thread"},
+        "e2e": {"value": round(tps, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=HEADLINE, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--secondary", default=SECONDARY, help="extra config in the same line ('' = none)")
+    ap.add_argument("--ncopy", type=int, default=8)
+    ap.add_argument("--nbatch", type=int, default=8)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    pk, pk_kind = peaks()
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if "CUDA_VISIBLE_DEVICES" in os.environ else local
+
+    if world > 1:
+        dist.barrier()
+    main_res = measure_config(args.config, device, args.warmup, args.steps, args.ncopy,
+                              args.nbatch, pk, pk_kind, gpu_index)
+    sec_res = None
+    if args.secondary and args.secondary != args.config:
+        sec_res = measure_config(args.secondary, device, args.warmup, max(3, args.steps // 10),
+                                 args.ncopy, args.nbatch, pk, pk_kind, gpu_index)
+    ms = main_res["ms"]
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    cfg = main_res["cfg"]
+    value = world * cfg.T / (ms * 1e-3)
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        n, sec = oracle_sample(cfg, args.cpu_budget, 10 ** 6)
+        cpu = {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} single tokens of {cfg.name} (router + {cfg.k} experts + shared), "
+                         f"{sec:.1f} s of single-thread CPU work"}
+
+    if rank == 0:
+        roof = gpu_roofline_decode(cfg, main_res["gu_ms"], main_res["active"], pk, pk_kind)
+        layer_gbs = main_res["layer_bytes"] / (ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "us_per_layer": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int4 weights x bf16 activations, f32 accumulate",
+            "data": "synthetic (seeded generator, random weights of the layer's shapes)",
+            "config": {
+                "workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, top-{cfg.k}, F={cfg.F}, "
+                            f"shared F={cfg.Fs}, int4 g{cfg.group}, seed {cfg.seed}",
+                "l2": f"inputs larger than L2: {main_res['packed_copies']} weight copies x "
+                      f"{main_res['batches']} activation batches rotated per step",
+                "timing": "CUDA graph replay of moe_layer_forward, CUDA events over the timed steps",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+            },
+            "roofline": roof,
+            "layer_roofline": {"bound": "hbm", "bytes_per_step": int(main_res["layer_bytes"]),
+                               "achieved": round(layer_gbs, 1), "peak": pk["hbm_gbs"],
+                               "unit": "GB/s", "frac": round(layer_gbs / pk["hbm_gbs"], 4)},
+            "active_experts_mean": float(np.mean(main_res["active"])),
+            "clocks": main_res["clocks"],
+            "e2e": {"value": round(cfg.T / (main_res["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
+                    "h2d_bytes_per_step": main_res["h2d"], "d2h_bytes_per_step": main_res["d2h"],
+                    "ms_per_step": round(main_res["e2e_ms"], 5),
+                    "mode": "graph replay of moe_layer_forward_host (pinned host x and out)"},
+            "gpu_launches": kernels_per_step(cfg) * args.steps,
+            "cpu_baseline": cpu,
+            "peaks": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback",
+        }
+        if sec_res is not None:
+            scfg = sec_res["cfg"]
+            sroof = gpu_roofline_prefill(scfg, sec_res["gu_ms"], pk, pk_kind)
+            tf = scfg.flops() / (sec_res["ms"] * 1e-3) / 1e12
+            line["secondary"] = {
+                "workload": f"{scfg.name}: T={scfg.T}, same layer shapes, seed {scfg.seed}",
+                "value": round(scfg.T / (sec_res["ms"] * 1e-3), 1), "unit": "tokens/s",
+                "us_per_layer": round(sec_res["ms"] * 1e3, 1),
+                "layer_tflops": round(tf, 2),
+                "layer_frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                "roofline": sroof, "clocks": sec_res["clocks"],
+                "e2e": {"value": round(scfg.T / (sec_res["e2e_ms"] * 1e-3), 1),
+                        "unit": "tokens/s", "h2d_bytes_per_step": sec_res["h2d"],
+                        "d2h_bytes_per_step": sec_res["d2h"]},
+            }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,242 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the GB300 (sm_103a) routed MoE FFN layer.
+ *
+ * The layer (thewafflehaus/butter PR #69, commit "feat(laguna): Laguna-S-2.1
+ * decode on the CUDA engine"): a sigmoid top-k router with a score-correction
+ * bias, routed experts with int4 weights and fused gate+up SwiGLU, a down
+ * projection, and a weighted combine plus an always-on shared expert.  The
+ * prefill form (same page, commit "feat(laguna): batched prefill with
+ * tensor-core projections, fused MoE, CTA scheduling") runs the experts as a
+ * grouped GEMM driven by on-device descriptors, largest expert first, with
+ * N-banded tile order for weight reuse in L2.
+ *
+ * Conventions shared by every call
+ *  - Pointers marked (device) are CUDA device memory owned by the caller; the
+ *    library allocates nothing, frees nothing and keeps no pointer after a
+ *    call returns.  Pointers marked (host) are host memory; pinned memory is
+ *    needed for the copies to overlap.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *    is asynchronous on that stream and performs no host synchronisation and
+ *    no host read of device data, so a sequence of calls can be captured into
+ *    a CUDA graph.  moe_check_device_status is the one exception (it syncs).
+ *  - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
+ *  - Argument errors are detected on the host before anything is launched and
+ *    returned synchronously; nothing is enqueued in that case.  A failed
+ *    launch returns MOE_ERR_CUDA.  Device-side consistency checks (an expert
+ *    id out of range, inconsistent counts) set a flag in the workspace instead
+ *    of trapping; moe_check_device_status reads it.
+ *  - T = 0 is valid: the call validates the other arguments, returns MOE_OK
+ *    and enqueues nothing.
+ *
+ * Numerics (the reading of the layer statement this library implements)
+ *  - int4 weights: per row, per group of `group` consecutive K elements,
+ *    s = fp16(absmax / 7) (absmax/7 evaluated in fp32, then rounded to fp16),
+ *    q = clamp(rint(w / s), -8, 7) (w/s in fp32, ties to even), s = 0 gives
+ *    q = 0.  Packed layout [rows][K/2] bytes: byte j holds element 2j in bits
+ *    0-3 and element 2j+1 in bits 4-7, two's complement.  Scales are fp16
+ *    [rows][K/group].  The dequantised weight is q * s, exactly.
+ *  - Router: l = x . W_r[e] (fp32 accumulate), s = sigmoid(l); the k experts
+ *    with the largest s + bias[e] are selected (ties to the lower id, listed
+ *    in descending order); combine weights w_j = s_j / sum_j s_j.  The bias
+ *    takes part in the selection only.
+ *  - Expert e on token t: g = x . w^_gate[f], u = x . w^_up[f] (fp32
+ *    accumulate), H = bf16(silu(g) * u); Y = H . w^_down[c] (fp32 accumulate).
+ *  - out[t] = bf16( sum_j w_tj * Y[pos(t, j)] + Y[shared row of t] ),
+ *    accumulated in fp32 in the order j = 0..k-1, then the shared expert.
+ *
+ * Row numbering of the expert intermediates H [rows][F] and Y [rows][d]:
+ * rows 0..T*k-1 are the routed slots in descriptor order (expert ascending,
+ * token ascending within an expert; row r belongs to slot perm[r]); rows
+ * T*k..T*k+T-1 are the shared expert's rows for tokens 0..T-1.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size      */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid, but outside the shapes the kernels handle */
+    MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required       */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime call or a kernel launch failed    */
+    MOE_ERR_DEVICE_CHECK = 5  /* a device-side consistency check tripped          */
+} moe_status_t;
+
+/* Layer dimensions.  Supported: d % 256 == 0, F % 128 == 0, F_s % 128 == 0,
+   group in {32, 64, 128} dividing d, F and F_s, 1 <= k <= min(E, 32),
+   1 <= E <= 1024, 0 <= T and T * (k + 1) < 2^31. */
+typedef struct {
+    int32_t T;      /* tokens in the batch                      */
+    int32_t d;      /* model width                              */
+    int32_t E;      /* routed experts                           */
+    int32_t k;      /* experts selected per token               */
+    int32_t F;      /* routed expert FFN width                  */
+    int32_t F_s;    /* shared expert FFN width                  */
+    int32_t group;  /* int4 quantisation group along K          */
+    uint32_t flags; /* MOE_FLAG_* below                         */
+} moe_dims_t;
+
+/* Path selection and scheduling switches (dims.flags). */
+#define MOE_FLAG_FORCE_GEMV 0x1u    /* run the experts on the CUDA-core GEMV path     */
+#define MOE_FLAG_FORCE_GROUPED 0x2u /* run the experts on the tcgen05 grouped path    */
+#define MOE_FLAG_NO_SCHED 0x4u      /* grouped path: expert-id order, no N-banding     */
+
+/* Packed int4 weights: q [rows][K/2] bytes, s [rows][K/group] fp16 (device). */
+typedef struct {
+    const uint8_t* q;
+    const uint16_t* s;
+} moe_w4_t;
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status_t status);
+
+/* ----------------------------------------------------------------------------
+ * moe_pack_w4 -- quantise fp32 weights to the packed int4 format above.
+ * Source: the Q4 re-quantised expert weights of thewafflehaus/butter PR #69
+ * (commit "feat(laguna): Laguna-S-2.1 decode on the CUDA engine"; weights are
+ * re-quantised at load).  Load-time, not on the per-token path.
+ *   w    (device) fp32 [rows][K], row-major
+ *   q    (device) out: uint8 [rows][K/2]
+ *   s    (device) out: fp16 bits [rows][K/group]
+ * Requires K % group == 0, group in {32, 64, 128}, rows >= 0.  Weights must be
+ * finite.  Returns MOE_ERR_UNSUPPORTED for other group sizes.
+ */
+moe_status_t moe_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group, uint8_t* q,
+                         uint16_t* s, void* stream);
+
+/* Bytes of workspace the per-step calls below need for these dimensions
+   (the same number serves every call; 0 on invalid dims). */
+size_t moe_workspace_bytes(const moe_dims_t* dims);
+
+/* ----------------------------------------------------------------------------
+ * moe_router_topk -- sigmoid router with score-correction bias, top-k.
+ * Source: the Laguna MoE router (sigmoid scores, ten experts per token, a
+ * correction bias added to the scores for the choice), thewafflehaus/butter
+ * PR #69, commit "feat(laguna): Laguna-S-2.1 decode on the CUDA engine".
+ *   x        (device) bf16 [T][d]
+ *   W_r      (device) fp32 [E][d]
+ *   bias     (device) fp32 [E]
+ *   topk_idx (device) out: int32 [T][k], descending s + bias
+ *   topk_w   (device) out: fp32 [T][k], s_j / sum_j s_j
+ *   margin   (device) out, nullable: fp32 [T], (k-th largest s + bias) minus
+ *            ((k+1)-th largest), +inf when k == E
+ *   ws       (device) workspace of moe_workspace_bytes(dims) bytes
+ */
+moe_status_t moe_router_topk(const uint16_t* x, const float* W_r, const float* bias,
+                             const moe_dims_t* dims, int32_t* topk_idx, float* topk_w,
+                             float* margin, void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * moe_build_descriptors -- on-device expert descriptors (counting sort).
+ * Source: the prefill MoE's expert descriptors, built on the device,
+ * thewafflehaus/butter PR #69, commit "feat(laguna): batched prefill with
+ * tensor-core projections, fused MoE, CTA scheduling"; CSR offsets with one
+ * entry per expert plus one and a router-sorted token index, thewafflehaus/
+ * FFAI PR #72 (Nemotron W4A16 Marlin MoE commit).
+ *   topk_idx (device) int32 [T][k], every id in [0, E)
+ *   counts   (device) out: int32 [E], slots per expert
+ *   offsets  (device) out: int32 [E+1], exclusive scan of counts
+ *   perm     (device) out: int32 [T*k], slot ids t*k+j sorted by (expert, token)
+ *   pos      (device) out: int32 [T*k], pos[perm[r]] = r
+ *   sched    (device) out: int32 [E], experts by count, largest first, ties to
+ *            the lower id
+ *   ws       (device) workspace; also receives the tile schedule that
+ *            moe_gateup_swiglu_w4a16 and moe_down_w4a16 read, so pass the same
+ *            workspace to them for this batch.
+ * An id outside [0, E) sets the device check flag (see moe_check_device_status)
+ * and the slot is dropped from the descriptors.
+ */
+moe_status_t moe_build_descriptors(const int32_t* topk_idx, const moe_dims_t* dims,
+                                   int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
+                                   int32_t* sched, void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * moe_gateup_swiglu_w4a16 -- fused gate+up projection with SwiGLU, every
+ * selected expert plus the shared expert, reading x through perm (gather on
+ * read).  Source: the fused gate+up MoE projection, with the shared expert
+ * run through the same gathered kernel, thewafflehaus/butter PR #69, commit
+ * "feat(laguna): Laguna-S-2.1 decode on the CUDA engine"; gate and up stacked
+ * per expert in the prefill path, commit "feat(laguna): batched prefill with
+ * tensor-core projections, fused MoE, CTA scheduling".
+ *   x        (device) bf16 [T][d]
+ *   offsets, perm, sched (device) from moe_build_descriptors
+ *   Wgu      routed gate+up, q [E][2F][d/2], s [E][2F][d/group]; rows 0..F-1
+ *            of each expert are the gate, rows F..2F-1 the up projection
+ *   Wgu_s    shared gate+up, q [2F_s][d/2], s [2F_s][d/group]
+ *   H        (device) out: bf16 [T*k + T][max(F, F_s)] (row stride max(F, F_s))
+ *   ws       the workspace moe_build_descriptors filled for this batch
+ * T <= 64 runs a CUDA-core GEMV, larger T the tcgen05 grouped kernel (the
+ * flags can force either).
+ */
+moe_status_t moe_gateup_swiglu_w4a16(const uint16_t* x, const moe_dims_t* dims,
+                                     const int32_t* offsets, const int32_t* perm,
+                                     const int32_t* sched, moe_w4_t Wgu, moe_w4_t Wgu_s,
+                                     uint16_t* H, void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * moe_down_w4a16 -- down projection of every row of H.
+ * Source: the per-expert down projection of the same pages' MoE layer.
+ *   H        (device) bf16 [T*k + T][max(F, F_s)]
+ *   offsets, sched (device) from moe_build_descriptors
+ *   Wd       routed down, q [E][d][F/2], s [E][d][F/group]
+ *   Wd_s     shared down, q [d][F_s/2], s [d][F_s/group]
+ *   Y        (device) out: fp32 [T*k + T][d]
+ *   ws       the workspace moe_build_descriptors filled for this batch
+ */
+moe_status_t moe_down_w4a16(const uint16_t* H, const moe_dims_t* dims, const int32_t* offsets,
+                            const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * moe_combine_shared -- weighted combine of the routed rows plus the shared
+ * row, fixed summation order (deterministic).  Source: the deterministic
+ * scatter-add and the residual + routed + shared add of thewafflehaus/FFAI
+ * PR #72 (Nemotron commits "ffai_add3" and W4A16 Marlin MoE).
+ *   Y        (device) fp32 [T*k + T][d]
+ *   topk_w   (device) fp32 [T][k]
+ *   pos      (device) int32 [T*k]
+ *   out      (device) out: bf16 [T][d]
+ */
+moe_status_t moe_combine_shared(const float* Y, const float* topk_w, const int32_t* pos,
+                                const moe_dims_t* dims, uint16_t* out, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * moe_layer_forward -- the whole layer in one call: router, descriptors,
+ * gate+up SwiGLU, down, combine, with the intermediates in the workspace.
+ * Same arguments as the calls above; ws must hold moe_layer_workspace_bytes.
+ * Graph-capturable.
+ */
+size_t moe_layer_workspace_bytes(const moe_dims_t* dims);
+moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float* bias,
+                               const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd,
+                               moe_w4_t Wgu_s, moe_w4_t Wd_s, uint16_t* out, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* moe_layer_forward_host -- as moe_layer_forward, but x_host is read from
+ * host memory and the output is written to out_host: the call enqueues the
+ * host-to-device copy of x, the layer and the device-to-host copy of out on
+ * `stream` and returns without waiting (the caller synchronises the stream
+ * before reading out_host).  Both host buffers should be pinned.  The device
+ * staging buffers for x and out are part of moe_layer_workspace_bytes. */
+moe_status_t moe_layer_forward_host(const uint16_t* x_host, const float* W_r, const float* bias,
+                                    const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd,
+                                    moe_w4_t Wgu_s, moe_w4_t Wd_s, uint16_t* out_host, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/* moe_check_device_status -- synchronises `stream`, reads and clears the
+ * device check flag in `ws`.  Returns MOE_ERR_DEVICE_CHECK if a kernel
+ * recorded an inconsistency since the last check, MOE_ERR_CUDA if the stream
+ * reported an error, MOE_OK otherwise.  For tests and debugging; it is the one
+ * call that blocks the host. */
+moe_status_t moe_check_device_status(void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,328 @@
+// extern "C" entry points of libmoe.so: argument validation, workspace
+// layout, path dispatch.  Every entry point validates on the host, then
+// enqueues kernels on the caller's stream; none allocates or synchronises
+// (moe_check_device_status excepted).
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+
+WsLayout ws_layout(const moe_dims_t& d) {
+    WsLayout L{};
+    const int64_t T = d.T, E = d.E, k = d.k;
+    const int64_t slots = T * k;
+    const int64_t rows = slots + T;
+    const int64_t Fmax = std::max(d.F, d.F_s);
+    L.router_ksplit = (d.d % 512 == 0) ? d.d / 512 : d.d / 256;
+    const int64_t ks = T <= kRouterSmallT ? L.router_ksplit : 1;
+    // tile lists: one entry per (group, 128-row weight band, 128-token tile)
+    const int64_t groups = std::min<int64_t>(E, slots) + 1;
+    const int64_t tok_tiles = (slots + kTileN - 1) / kTileN + groups + (T + kTileN - 1) / kTileN;
+    const int64_t bands = (std::max<int64_t>(d.d, 2 * Fmax) + kTileM - 1) / kTileM;
+    L.max_tiles = tok_tiles * bands;
+
+    size_t off = 0;
+    L.header = off;
+    off += align256(sizeof(WsHeader));
+    L.logits = off;
+    off += align256(sizeof(float) * (size_t)(ks * T * E));
+    L.tiles = off;
+    off += align256(sizeof(int4) * (size_t)(2 * L.max_tiles));
+    L.step_bytes = off;
+
+    L.topk_idx = off;
+    off += align256(sizeof(int32_t) * (size_t)slots);
+    L.topk_w = off;
+    off += align256(sizeof(float) * (size_t)slots);
+    L.counts = off;
+    off += align256(sizeof(int32_t) * (size_t)E);
+    L.offsets = off;
+    off += align256(sizeof(int32_t) * (size_t)(E + 1));
+    L.perm = off;
+    off += align256(sizeof(int32_t) * (size_t)slots);
+    L.pos = off;
+    off += align256(sizeof(int32_t) * (size_t)slots);
+    L.sched = off;
+    off += align256(sizeof(int32_t) * (size_t)E);
+    L.H = off;
+    off += align256(sizeof(uint16_t) * (size_t)(rows * Fmax));
+    L.Y = off;
+    off += align256(sizeof(float) * (size_t)(rows * d.d));
+    L.x_stage = off;
+    off += align256(sizeof(uint16_t) * (size_t)(T * d.d));
+    L.out_stage = off;
+    off += align256(sizeof(uint16_t) * (size_t)(T * d.d));
+    L.layer_bytes = off;
+    return L;
+}
+
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    // per (kernel, device) once; a small table is enough for the handful of kernels
+    static std::mutex mu;
+    static const void* seen_k[64];
+    static int seen_dev[64];
+    static size_t seen_bytes[64];
+    static int n_seen = 0;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_seen; ++i)
+        if (seen_k[i] == kernel && seen_dev[i] == dev && seen_bytes[i] >= bytes) return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err != cudaSuccess) return err;
+    if (n_seen < 64) {
+        seen_k[n_seen] = kernel;
+        seen_dev[n_seen] = dev;
+        seen_bytes[n_seen] = bytes;
+        ++n_seen;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+moe_status_t map_err(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool group_ok(int g) { return g == 32 || g == 64 || g == 128; }
+
+// Shape validation shared by the per-step calls.
+moe_status_t check_dims(const moe_dims_t* d) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->d <= 0 || d->E <= 0 || d->k <= 0 || d->F <= 0 || d->F_s <= 0 ||
+        d->group <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (d->k > d->E) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)d->T * (d->k + 1) >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
+    if (!group_ok(d->group)) return MOE_ERR_UNSUPPORTED;
+    if (d->d % 256 || d->F % 128 || d->F_s % 128) return MOE_ERR_UNSUPPORTED;
+    if (d->d % d->group || d->F % d->group || d->F_s % d->group) return MOE_ERR_UNSUPPORTED;
+    if (d->k > 32 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
+    if ((d->flags & MOE_FLAG_FORCE_GEMV) && (d->flags & MOE_FLAG_FORCE_GROUPED))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) % 256) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+bool w4_ok(moe_w4_t w) { return w.q && w.s; }
+
+template <typename T>
+T* ws_at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+bool use_gemv(const moe_dims_t& d) {
+    if (d.flags & MOE_FLAG_FORCE_GEMV) return true;
+    if (d.flags & MOE_FLAG_FORCE_GROUPED) return false;
+    return d.T <= kGemvMaxT;
+}
+
+moe_status_t gateup_impl(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,
+                         const int32_t* perm, const int32_t* sched, moe_w4_t Wgu, moe_w4_t Wgu_s,
+                         uint16_t* H, void* ws, cudaStream_t st) {
+    WsHeader* hdr = ws_at<WsHeader>(ws, ws_layout(d).header);
+    if (use_gemv(d) || true)
+        return map_err(launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, hdr, st));
+    return MOE_ERR_UNSUPPORTED;
+}
+
+moe_status_t down_impl(const uint16_t* H, const moe_dims_t& d, const int32_t* offsets,
+                       const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y, void* ws,
+                       cudaStream_t st) {
+    WsHeader* hdr = ws_at<WsHeader>(ws, ws_layout(d).header);
+    if (use_gemv(d) || true)
+        return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, hdr, st));
+    return MOE_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null pointer or inconsistent size";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape outside the supported set";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
+        case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK: a device-side check tripped";
+    }
+    return "unknown moe_status_t";
+}
+
+moe_status_t moe_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group, uint8_t* q,
+                         uint16_t* s, void* stream) {
+    if (rows < 0 || K <= 0 || group <= 0) return MOE_ERR_INVALID_ARG;
+    if (!group_ok(group)) return MOE_ERR_UNSUPPORTED;
+    if (K % group) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!w || !q || !s) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(w) % 16 || reinterpret_cast<uintptr_t>(q) % 4 ||
+        reinterpret_cast<uintptr_t>(s) % 2)
+        return MOE_ERR_INVALID_ARG;
+    return map_err(launch_pack_w4(w, rows, K, group, q, s, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_workspace_bytes(const moe_dims_t* dims) {
+    if (check_dims(dims) != MOE_OK) return 0;
+    return ws_layout(*dims).step_bytes;
+}
+
+size_t moe_layer_workspace_bytes(const moe_dims_t* dims) {
+    if (check_dims(dims) != MOE_OK) return 0;
+    return ws_layout(*dims).layer_bytes;
+}
+
+moe_status_t moe_router_topk(const uint16_t* x, const float* W_r, const float* bias,
+                             const moe_dims_t* dims, int32_t* topk_idx, float* topk_w,
+                             float* margin, void* ws, size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.step_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!x || !W_r || !bias || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    return map_err(launch_router(x, W_r, bias, *dims, topk_idx, topk_w, margin,
+                                 ws_at<float>(ws, L.logits), L.router_ksplit,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_build_descriptors(const int32_t* topk_idx, const moe_dims_t* dims,
+                                   int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
+                                   int32_t* sched, void* ws, size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.step_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!topk_idx || !counts || !offsets || !perm || !pos || !sched) return MOE_ERR_INVALID_ARG;
+    return map_err(launch_descriptors(topk_idx, *dims, counts, offsets, perm, pos, sched,
+                                      ws_at<WsHeader>(ws, L.header), ws_at<int4>(ws, L.tiles),
+                                      L.max_tiles, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_gateup_swiglu_w4a16(const uint16_t* x, const moe_dims_t* dims,
+                                     const int32_t* offsets, const int32_t* perm,
+                                     const int32_t* sched, moe_w4_t Wgu, moe_w4_t Wgu_s,
+                                     uint16_t* H, void* ws, size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.step_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!x || !offsets || !perm || !sched || !H || !w4_ok(Wgu) || !w4_ok(Wgu_s))
+        return MOE_ERR_INVALID_ARG;
+    return gateup_impl(x, *dims, offsets, perm, sched, Wgu, Wgu_s, H, ws,
+                       static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_down_w4a16(const uint16_t* H, const moe_dims_t* dims, const int32_t* offsets,
+                            const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y, void* ws,
+                            size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.step_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!H || !offsets || !sched || !Y || !w4_ok(Wd) || !w4_ok(Wd_s)) return MOE_ERR_INVALID_ARG;
+    return down_impl(H, *dims, offsets, sched, Wd, Wd_s, Y, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine_shared(const float* Y, const float* topk_w, const int32_t* pos,
+                                const moe_dims_t* dims, uint16_t* out, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!Y || !topk_w || !pos || !out) return MOE_ERR_INVALID_ARG;
+    return map_err(launch_combine(Y, topk_w, pos, *dims, out, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float* bias,
+                               const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd,
+                               moe_w4_t Wgu_s, moe_w4_t Wd_s, uint16_t* out, void* ws,
+                               size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.layer_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!x || !W_r || !bias || !out || !w4_ok(Wgu) || !w4_ok(Wd) || !w4_ok(Wgu_s) || !w4_ok(Wd_s))
+        return MOE_ERR_INVALID_ARG;
+    const moe_dims_t& d = *dims;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* topk_idx = ws_at<int32_t>(ws, L.topk_idx);
+    float* topk_w = ws_at<float>(ws, L.topk_w);
+    int32_t* counts = ws_at<int32_t>(ws, L.counts);
+    int32_t* offsets = ws_at<int32_t>(ws, L.offsets);
+    int32_t* perm = ws_at<int32_t>(ws, L.perm);
+    int32_t* pos = ws_at<int32_t>(ws, L.pos);
+    int32_t* sched = ws_at<int32_t>(ws, L.sched);
+    uint16_t* H = ws_at<uint16_t>(ws, L.H);
+    float* Y = ws_at<float>(ws, L.Y);
+    WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
+    cudaError_t e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
+                                  ws_at<float>(ws, L.logits), L.router_ksplit, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
+                           ws_at<int4>(ws, L.tiles), L.max_tiles, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if ((st = gateup_impl(x, d, offsets, perm, sched, Wgu, Wgu_s, H, ws, s)) != MOE_OK) return st;
+    if ((st = down_impl(H, d, offsets, sched, Wd, Wd_s, Y, ws, s)) != MOE_OK) return st;
+    return map_err(launch_combine(Y, topk_w, pos, d, out, s));
+}
+
+moe_status_t moe_layer_forward_host(const uint16_t* x_host, const float* W_r, const float* bias,
+                                    const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd,
+                                    moe_w4_t Wgu_s, moe_w4_t Wd_s, uint16_t* out_host, void* ws,
+                                    size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.layer_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = sizeof(uint16_t) * (size_t)dims->T * dims->d;
+    uint16_t* xd = ws_at<uint16_t>(ws, L.x_stage);
+    uint16_t* od = ws_at<uint16_t>(ws, L.out_stage);
+    if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    st = moe_layer_forward(xd, W_r, bias, dims, Wgu, Wd, Wgu_s, Wd_s, od, ws, ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    if (cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status_t moe_check_device_status(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws || ws_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    int32_t flags = 0;
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    if (cudaMemcpy(&flags, &hdr->error_flags, sizeof(flags), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (flags) {
+        const int32_t zero = 0;
+        if (cudaMemcpy(&hdr->error_flags, &zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_ERR_DEVICE_CHECK;
+    }
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+// Internal definitions shared by the CUDA translation units of libmoe.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Device check flags, recorded in the workspace header instead of trapping.
+enum : int32_t {
+    kErrBadExpertId = 1 << 0,    // a topk id outside [0, E)
+    kErrCountMismatch = 1 << 1,  // descriptor counts do not add up to T*k
+    kErrWaitTimeout = 1 << 2,    // a bounded spin-wait gave up
+    kErrBadTile = 1 << 3,        // a tile index outside its bounds
+};
+
+// Workspace header: the first 256 bytes of every workspace.
+struct WsHeader {
+    int32_t error_flags;   // OR of kErr* bits; cleared by moe_check_device_status
+    int32_t n_active;      // routed experts with count > 0 (written by the descriptors)
+    int32_t n_tiles[2];    // grouped-GEMM tile counts: [0] gate+up, [1] down
+    int32_t queue[4];      // work-queue counters of persistent kernels (reset per batch)
+    int32_t done[4];       // completion counters (reset by their last user)
+    int32_t pad[52];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+__device__ __forceinline__ void record_error(WsHeader* h, int32_t bit) {
+    if (h) atomicOr(&h->error_flags, bit);
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout.  Offsets are 256-byte aligned.
+struct WsLayout {
+    // per-step workspace (moe_workspace_bytes)
+    size_t header;        // WsHeader
+    size_t logits;        // fp32 [ksplit][T][E] router logit partials
+    size_t tiles;         // int4 tile descriptors of the grouped kernels
+    size_t step_bytes;
+    // whole-layer workspace (moe_layer_workspace_bytes) adds the intermediates
+    size_t topk_idx, topk_w, counts, offsets, perm, pos, sched, H, Y, x_stage, out_stage;
+    size_t layer_bytes;
+    int router_ksplit;    // K split of the small-T router
+    int64_t max_tiles;    // capacity of each tile list
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Router tiling: T <= kRouterSmallT uses the split-K GEMV form.
+constexpr int kRouterSmallT = 64;
+constexpr int kRouterKChunk = 1024;
+
+// GEMV (decode) expert path for T <= kGemvMaxT unless forced.
+constexpr int kGemvMaxT = 64;
+
+// Grouped-GEMM tile geometry (weight rows x tokens).
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+
+WsLayout ws_layout(const moe_dims_t& d);
+
+// ---------------------------------------------------------------------------
+// Launchers (defined in the .cu files).  All enqueue on `st` and return the
+// cudaGetLastError of the launch.
+cudaError_t launch_pack_w4(const float* w, int64_t rows, int64_t K, int group, uint8_t* q,
+                           uint16_t* s, cudaStream_t st);
+
+cudaError_t launch_router(const uint16_t* x, const float* W_r, const float* bias,
+                          const moe_dims_t& d, int32_t* topk_idx, float* topk_w, float* margin,
+                          float* logits, int ksplit, cudaStream_t st);
+
+cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int32_t* counts,
+                               int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,
+                               WsHeader* hdr, int4* tiles, int64_t max_tiles, cudaStream_t st);
+
+cudaError_t launch_gateup_gemv(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,
+                               const int32_t* perm, const int32_t* sched, moe_w4_t Wgu,
+                               moe_w4_t Wgu_s, uint16_t* H, WsHeader* hdr, cudaStream_t st);
+
+cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32_t* offsets,
+                             const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y,
+                             WsHeader* hdr, cudaStream_t st);
+
+cudaError_t launch_combine(const float* Y, const float* topk_w, const int32_t* pos,
+                           const moe_dims_t& d, uint16_t* out, cudaStream_t st);
+
+// Raise a kernel's dynamic shared-memory limit when `bytes` exceeds the 48 KB
+// default (once per kernel and device; safe to call during stream capture).
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
+// ---------------------------------------------------------------------------
+// Small device helpers.
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) {
+    return __uint_as_float(pair & 0xFFFF0000u);
+}
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+    __nv_bfloat16 b = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace moe

@@ -1,0 +1,74 @@
+// int4 weight packing (load-time).
+//
+// The Laguna expert weights are 4-bit, re-quantised when the model is loaded
+// (thewafflehaus/butter PR #69, commit "feat(laguna): Laguna-S-2.1 decode on
+// the CUDA engine").  Format: per row, per group of `group` consecutive K
+// elements, s = fp16(absmax / 7) and q = clamp(rint(w / s), -8, 7); byte j of a
+// row holds element 2j in bits 0-3 and element 2j+1 in bits 4-7.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// One thread per (row, group).  Reads `group` floats with 16-byte loads and
+// writes group/8 32-bit words of nibbles plus one fp16 scale.
+template <int G>
+__global__ void __launch_bounds__(256) pack_w4_kernel(const float* __restrict__ w, int64_t rows,
+                                                      int64_t K, uint8_t* __restrict__ q,
+                                                      __half* __restrict__ s) {
+    const int64_t ngroups = K / G;
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= rows * ngroups) return;
+    const int64_t r = gid / ngroups;
+    const int64_t g = gid - r * ngroups;
+    const float4* src = reinterpret_cast<const float4*>(w + r * K + g * G);
+
+    float amax = 0.0f;
+#pragma unroll 8
+    for (int i = 0; i < G / 4; ++i) {
+        float4 v = __ldg(src + i);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    const __half sh = __float2half_rn(__fdiv_rn(amax, 7.0f));
+    const float sf = __half2float(sh);
+
+    uint32_t* dst = reinterpret_cast<uint32_t*>(q + r * (K / 2) + g * (G / 2));
+#pragma unroll 4
+    for (int i = 0; i < G / 8; ++i) {
+        float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
+        float e[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            int qi = 0;
+            if (sf != 0.0f) {
+                float t = rintf(__fdiv_rn(e[j], sf));
+                t = fminf(fmaxf(t, -8.0f), 7.0f);
+                qi = (int)t;
+            }
+            word |= ((uint32_t)qi & 0xFu) << (4 * j);
+        }
+        dst[i] = word;
+    }
+    s[gid] = sh;
+}
+
+}  // namespace
+
+cudaError_t launch_pack_w4(const float* w, int64_t rows, int64_t K, int group, uint8_t* q,
+                           uint16_t* s, cudaStream_t st) {
+    const int64_t n = rows * (K / group);
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+    __half* sh = reinterpret_cast<__half*>(s);
+    switch (group) {
+        case 32: pack_w4_kernel<32><<<blocks, threads, 0, st>>>(w, rows, K, q, sh); break;
+        case 64: pack_w4_kernel<64><<<blocks, threads, 0, st>>>(w, rows, K, q, sh); break;
+        case 128: pack_w4_kernel<128><<<blocks, threads, 0, st>>>(w, rows, K, q, sh); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -8,15 +8,18 @@
  *
  * What the layer is, and where it is stated:
  *  - thewafflehaus/butter PR #69, commit "feat(laguna): Laguna-S-2.1 decode on
- *    the CUDA engine": the MoE layer is a sigmoid top-10 router with
- *    score-correction bias and a shared expert; expert weights are Q4
- *    (re-quantised at load); gate and up are fused (SwiGLU).
+ *    the CUDA engine": each token's MoE layer picks ten experts from sigmoid
+ *    router scores shifted by a correction bias, and adds a shared expert;
+ *    expert weights are 4-bit, re-quantised when the model is loaded; the
+ *    gate and up projections run fused (SwiGLU).
  *  - same page, commit "feat(laguna): batched prefill with tensor-core
- *    projections, fused MoE, CTA scheduling": grouped-GEMM MoE with on-device
- *    descriptors (per-expert counts, offsets and a token order), fused gate+up
- *    expert stacks, a W4A16 shared expert.
- *  - thewafflehaus/FFAI PR #72, Nemotron W4A16 Marlin MoE commit: CSR offsets
- *    [n_exp+1], router-sorted token indices, deterministic scatter-add.
+ *    projections, fused MoE, CTA scheduling": in prefill the experts run as a
+ *    grouped GEMM over descriptors built on the device (per-expert counts,
+ *    offsets and a token order), with gate and up stacked per expert and the
+ *    shared expert also in W4A16.
+ *  - thewafflehaus/FFAI PR #72, Nemotron W4A16 Marlin MoE commit: offsets in
+ *    CSR form (one per expert plus one), a router-sorted token index, and a
+ *    deterministic scatter-add of the expert outputs.
  *  - the layer statement accompanying the pages fixes the rest: the bias is
  *    used for selection only; combine weights are the selected sigmoid scores
  *    normalised to sum 1; int4 symmetric per group along K with

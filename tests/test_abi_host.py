@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads, every
+symbol include/moe.h declares is exported, and argument validation returns its
+documented status codes before anything would be launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_expert_layer_sigmoid_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import moe_expert_layer_sigmoid_gb300.build as b
+    b.build()
+    return moe.lib()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(moe.EXPORTS)
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert moe.status_string(code).startswith("MOE_")
+    assert "unknown" in moe.status_string(99)
+
+
+def _dims(**kw):
+    base = dict(T=4, d=256, E=16, k=2, F=128, F_s=128, group=32, flags=0)
+    base.update(kw)
+    return moe.Dims(**base)
+
+
+def test_workspace_bytes(L):
+    d = _dims()
+    a = moe.moe_workspace_bytes(d)
+    b = moe.moe_layer_workspace_bytes(d)
+    assert 256 <= a < b
+    assert moe.moe_workspace_bytes(_dims(T=4096)) > a
+    assert moe.moe_workspace_bytes(_dims(group=48)) == 0
+    assert moe.moe_workspace_bytes(_dims(k=17, E=16)) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(group=48), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d=300), moe.MOE_ERR_UNSUPPORTED),
+    (dict(F=96), moe.MOE_ERR_UNSUPPORTED),
+    (dict(k=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(k=20, E=16), moe.MOE_ERR_INVALID_ARG),
+    (dict(k=33, E=64), moe.MOE_ERR_UNSUPPORTED),
+    (dict(E=2048, k=4), moe.MOE_ERR_UNSUPPORTED),
+    (dict(T=-1), moe.MOE_ERR_INVALID_ARG),
+    (dict(flags=3), moe.MOE_ERR_INVALID_ARG),
+])
+def test_dims_validation(L, kw, code):
+    d = _dims(**kw)
+    ws = ctypes.create_string_buffer(1 << 20)
+    got = L.moe_router_topk(None, None, None, ctypes.byref(d), None, None, None,
+                            ctypes.addressof(ws), 1 << 20, None)
+    assert got == code
+
+
+def test_workspace_too_small(L):
+    d = _dims()
+    need = moe.moe_workspace_bytes(d)
+    got = L.moe_build_descriptors(None, ctypes.byref(d), None, None, None, None, None, None,
+                                  need, None)
+    assert got == moe.MOE_ERR_WORKSPACE
+    got = L.moe_build_descriptors(None, ctypes.byref(d), None, None, None, None, None, 256, 16,
+                                  None)
+    assert got == moe.MOE_ERR_WORKSPACE
+
+
+def test_null_pointers_rejected(L):
+    d = _dims()
+    need = moe.moe_layer_workspace_bytes(d)
+    fake_ws = 1 << 20  # never dereferenced: validation fails first
+    assert L.moe_layer_forward(None, None, None, ctypes.byref(d), moe.W4(), moe.W4(), moe.W4(),
+                               moe.W4(), None, fake_ws, need, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_shared(None, None, None, ctypes.byref(d), None,
+                                None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_pack_validation(L):
+    assert L.moe_pack_w4(None, 4, 96, 48, None, None, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_pack_w4(None, 4, 100, 32, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pack_w4(None, 0, 128, 32, None, None, None) == moe.MOE_OK
+    assert L.moe_pack_w4(None, 4, 128, 32, None, None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_zero_tokens_validates_then_returns_ok(L):
+    d = _dims(T=0)
+    need = moe.moe_layer_workspace_bytes(d)
+    ws = 1 << 20
+    assert L.moe_layer_forward(None, None, None, ctypes.byref(d), moe.W4(), moe.W4(), moe.W4(),
+                               moe.W4(), None, ws, need, None) == moe.MOE_OK
+    bad = _dims(T=0, group=48)
+    assert L.moe_layer_forward(None, None, None, ctypes.byref(bad), moe.W4(), moe.W4(), moe.W4(),
+                               moe.W4(), None, ws, need, None) == moe.MOE_ERR_UNSUPPORTED

@@ -7,8 +7,9 @@ quantised by whichever side (oracle or CUDA) consumes them.
 
 Shapes follow the Laguna-S-2.1 MoE layer as the decode commit of
 thewafflehaus/butter PR #69 ("feat(laguna): Laguna-S-2.1 decode on the CUDA
-engine") describes it: a sigmoid top-10 router with score-correction bias over
-256 routed experts plus one shared expert; d_model 4096, expert FFN 1024.
+engine") describes it: sigmoid router scores with a correction bias choose ten
+of 256 routed experts per token, and one shared expert always runs; here
+d_model 4096 and expert FFN 1024.
 Value recipe (the layer statement that accompanies the pages):
   x ~ N(0, 1) rounded to bf16; W_r ~ N(0, 1/d) fp32; bias ~ N(0, 0.5) fp32;
   expert weights ~ N(0, 1/K) fp32, K the contraction length (d for gate/up,

@@ -11,7 +11,8 @@
  *   key   = mix64(seed * phi + mix64(tid + c0))
  *   h(i)  = mix64(key + (i + 1) * phi)
  *   U(i)  = ((h(i) >> 11) + 0.5) * 2^-53            uniform on (0, 1)
- *   N(i)  = sqrt(-2 ln U(2i)) * cos(2 pi U(2i+1))   Box & Muller (1958), cosine branch
+ *   N(2m)   = sqrt(-2 ln U(2m)) * cos(2 pi U(2m+1))  Box & Muller (1958); both
+ *   N(2m+1) = sqrt(-2 ln U(2m)) * sin(2 pi U(2m+1))  outputs of the pair are used
  * mix64 is the 64-bit finaliser of SplitMix64 (Steele, Lea & Flood, "Fast
  * splittable pseudorandom number generators", OOPSLA 2014), phi = 2^64 / golden ratio.
  * Everything is evaluated in double; a value is converted to fp32 (and, for
@@ -38,12 +39,30 @@ static double unit_open(uint64_t key, uint64_t i) {
     return ((double)(h >> 11) + 0.5) * (1.0 / 9007199254740992.0);
 }
 
-static double std_normal(uint64_t key, uint64_t i) {
+/* The Box-Muller pair m: out[0] = N(2m), out[1] = N(2m+1). */
+static void normal_pair(uint64_t key, uint64_t m, double out[2]) {
     const double two_pi = 6.283185307179586476925286766559;
-    double u1 = unit_open(key, 2 * i);
-    double u2 = unit_open(key, 2 * i + 1);
-    return sqrt(-2.0 * log(u1)) * cos(two_pi * u2);
+    double u1 = unit_open(key, 2 * m);
+    double u2 = unit_open(key, 2 * m + 1);
+    double r = sqrt(-2.0 * log(u1));
+    out[0] = r * cos(two_pi * u2);
+    out[1] = r * sin(two_pi * u2);
 }
+
+/* Calls emit(j, N(start + j)) for j in [0, n). */
+#define FOR_EACH_NORMAL(key, start, n, BODY)                       \
+    do {                                                           \
+        uint64_t i_ = (start), end_ = (start) + (n);               \
+        double p_[2];                                              \
+        while (i_ < end_) {                                        \
+            normal_pair((key), i_ / 2, p_);                        \
+            for (int h_ = (int)(i_ & 1); h_ < 2 && i_ < end_; ++h_, ++i_) { \
+                const uint64_t j = i_ - (start);                   \
+                const double v = p_[h_];                           \
+                BODY;                                              \
+            }                                                      \
+        }                                                          \
+    } while (0)
 
 /* bf16 bit pattern of a finite fp32 value, round to nearest even. */
 static uint16_t f32_to_bf16_bits(float f) {
@@ -57,15 +76,14 @@ static uint16_t f32_to_bf16_bits(float f) {
 void gen_normal_f32(uint64_t seed, uint64_t tid, uint64_t start, uint64_t n, double std,
                     float* out) {
     uint64_t key = tensor_key(seed, tid);
-    for (uint64_t j = 0; j < n; ++j) out[j] = (float)(std * std_normal(key, start + j));
+    FOR_EACH_NORMAL(key, start, n, out[j] = (float)(std * v));
 }
 
 /* out[j] = bf16 bits of (float)(std * N(start + j)). */
 void gen_normal_bf16(uint64_t seed, uint64_t tid, uint64_t start, uint64_t n, double std,
                      uint16_t* out) {
     uint64_t key = tensor_key(seed, tid);
-    for (uint64_t j = 0; j < n; ++j)
-        out[j] = f32_to_bf16_bits((float)(std * std_normal(key, start + j)));
+    FOR_EACH_NORMAL(key, start, n, out[j] = f32_to_bf16_bits((float)(std * v)));
 }
 
 /* A seeded permutation of 0..n-1 (Fisher & Yates, Durstenfeld's in-place form). */
