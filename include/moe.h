@@ -104,8 +104,9 @@ const char* moe_status_string(moe_status_t status);
  *   w    (device) fp32 [rows][K], row-major
  *   q    (device) out: uint8 [rows][K/2]
  *   s    (device) out: fp16 bits [rows][K/group]
- * Requires K % group == 0, group in {32, 64, 128}, rows >= 0.  Weights must be
- * finite.  Returns MOE_ERR_UNSUPPORTED for other group sizes.
+ * Requires K % group == 0, group in {8, 16, 32, 64, 128} (the layer calls take
+ * 32, 64 or 128), rows >= 0, w 16-byte aligned.  Weights must be finite.
+ * Returns MOE_ERR_UNSUPPORTED for other group sizes.
  */
 moe_status_t moe_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group, uint8_t* q,
                          uint16_t* s, void* stream);

@@ -166,7 +166,7 @@ const char* moe_status_string(moe_status_t s) {
 moe_status_t moe_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group, uint8_t* q,
                          uint16_t* s, void* stream) {
     if (rows < 0 || K <= 0 || group <= 0) return MOE_ERR_INVALID_ARG;
-    if (!group_ok(group)) return MOE_ERR_UNSUPPORTED;
+    if (!(group == 8 || group == 16 || group_ok(group))) return MOE_ERR_UNSUPPORTED;
     if (K % group) return MOE_ERR_INVALID_ARG;
     if (rows == 0) return MOE_OK;
     if (!w || !q || !s) return MOE_ERR_INVALID_ARG;

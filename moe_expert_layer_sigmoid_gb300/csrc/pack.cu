@@ -63,6 +63,8 @@ cudaError_t launch_pack_w4(const float* w, int64_t rows, int64_t K, int group, u
     const unsigned blocks = (unsigned)((n + threads - 1) / threads);
     __half* sh = reinterpret_cast<__half*>(s);
     switch (group) {
+        case 8: pack_w4_kernel<8><<<blocks, threads, 0, st>>>(w, rows, K, q, sh); break;
+        case 16: pack_w4_kernel<16><<<blocks, threads, 0, st>>>(w, rows, K, q, sh); break;
         case 32: pack_w4_kernel<32><<<blocks, threads, 0, st>>>(w, rows, K, q, sh); break;
         case 64: pack_w4_kernel<64><<<blocks, threads, 0, st>>>(w, rows, K, q, sh); break;
         case 128: pack_w4_kernel<128><<<blocks, threads, 0, st>>>(w, rows, K, q, sh); break;
