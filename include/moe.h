@@ -134,6 +134,36 @@ moe_status_t moe_router_topk(const uint16_t* x, const float* W_r, const float* b
                              float* margin, void* ws, size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------------------------
+ * moe_router_topk_noalloc -- moe_router_topk without a workspace, for callers
+ * that cannot allocate device memory when they call the router.  Examples: a
+ * host framework that owns every device allocation through its own pool and
+ * forbids side allocations; a serving process that reserved all of HBM for
+ * weights and caches at start-up.  The pages have no counterpart: this is a
+ * library convenience, not part of the layer they describe.
+ *
+ * Arguments and results are those of moe_router_topk, minus ws/ws_bytes; the
+ * caller still passes x, W_r, bias and the output buffers.  The router's
+ * scratch (its fp32 logit partials) lives in a fixed 4 MiB device array inside
+ * libmoe.so.  Every GPU that loads the library holds that array until the
+ * process exits.  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *  - Limit: the partials need ksplit * T * E * 4 bytes, where ksplit = d / 512
+ *    (d / 256 when d % 512 != 0) for T <= 64 and 1 above.  Anything beyond
+ *    4 MiB returns MOE_ERR_UNSUPPORTED before launching.  For E = 256 that is
+ *    T <= 64 in the decode form (at d <= 16384) and T <= 4096 above it.
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it.  Make
+ *    that first call before any stream capture.
+ *  - Sharing: every call uses the same array.  The call writes every partial
+ *    it reads, so nothing needs clearing between calls.  Calls that overlap on
+ *    the GPU (concurrent streams, or several host threads on one device)
+ *    race on the array: serialise them.
+ */
+moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* W_r, const float* bias,
+                                     const moe_dims_t* dims, int32_t* topk_idx, float* topk_w,
+                                     float* margin, void* stream);
+
+/* ----------------------------------------------------------------------------
  * moe_build_descriptors -- on-device expert descriptors (counting sort).
  * Source: the prefill MoE's expert descriptors, built on the device,
  * thewafflehaus/butter PR #69, commit "feat(laguna): batched prefill with

@@ -35,7 +35,7 @@ EXPORTS = (
     "moe_status_string", "moe_pack_w4", "moe_workspace_bytes", "moe_router_topk",
     "moe_build_descriptors", "moe_gateup_swiglu_w4a16", "moe_down_w4a16", "moe_combine_shared",
     "moe_layer_workspace_bytes", "moe_layer_forward", "moe_layer_forward_host",
-    "moe_check_device_status",
+    "moe_check_device_status", "moe_router_topk_noalloc",
 )
 
 
@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
         "moe_layer_forward": ([p, p, p, D, W4, W4, W4, W4, p, p, sz, p], i32),
         "moe_layer_forward_host": ([p, p, p, D, W4, W4, W4, W4, p, p, sz, p], i32),
         "moe_check_device_status": ([p, sz, p], i32),
+        "moe_router_topk_noalloc": ([p, p, p, D, p, p, p, p], i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -171,6 +172,17 @@ def moe_router_topk(x, W_r, bias, dims: Dims, topk_idx, topk_w, margin, ws, stre
         _dev(topk_idx, torch.int32, "topk_idx"), _dev(topk_w, torch.float32, "topk_w"),
         None if margin is None else _dev(margin, torch.float32, "margin"),
         _ptr(ws), ws.numel(), _stream(stream)), "moe_router_topk")
+
+
+def moe_router_topk_noalloc(x, W_r, bias, dims: Dims, topk_idx, topk_w, margin, stream=None):
+    """The router without a workspace: its scratch is a fixed device array inside the
+    library (see include/moe.h for the size limit and the sharing rules)."""
+    _check(lib().moe_router_topk_noalloc(
+        _dev(x, torch.int16, "x"), _dev(W_r, torch.float32, "W_r"),
+        _dev(bias, torch.float32, "bias"), ctypes.byref(dims),
+        _dev(topk_idx, torch.int32, "topk_idx"), _dev(topk_w, torch.float32, "topk_w"),
+        None if margin is None else _dev(margin, torch.float32, "margin"), _stream(stream)),
+        "moe_router_topk_noalloc")
 
 
 def moe_build_descriptors(topk_idx, dims: Dims, counts, offsets, perm, pos, sched, ws,
