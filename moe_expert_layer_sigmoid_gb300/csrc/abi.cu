@@ -123,28 +123,46 @@ T* ws_at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
-bool use_gemv(const moe_dims_t& d) {
-    if (d.flags & MOE_FLAG_FORCE_GEMV) return true;
-    if (d.flags & MOE_FLAG_FORCE_GROUPED) return false;
-    return d.T <= kGemvMaxT;
+// Expert path: CUDA-core GEMV for small T (or when forced), the tcgen05
+// grouped kernel otherwise.  Shapes the grouped kernel does not cover run on
+// the GEMV unless the grouped path is forced, which then reports UNSUPPORTED.
+enum class Path { kGemv, kGrouped, kUnsupported };
+
+Path expert_path(const moe_dims_t& d) {
+    if (d.flags & MOE_FLAG_FORCE_GEMV) return Path::kGemv;
+    const bool ok = grouped_supported(d);
+    if (d.flags & MOE_FLAG_FORCE_GROUPED) return ok ? Path::kGrouped : Path::kUnsupported;
+    return (d.T > kGemvMaxT && ok) ? Path::kGrouped : Path::kGemv;
 }
 
 moe_status_t gateup_impl(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,
                          const int32_t* perm, const int32_t* sched, moe_w4_t Wgu, moe_w4_t Wgu_s,
                          uint16_t* H, void* ws, cudaStream_t st) {
-    WsHeader* hdr = ws_at<WsHeader>(ws, ws_layout(d).header);
-    if (use_gemv(d) || true)
-        return map_err(launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, hdr, st));
-    return MOE_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(d);
+    WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
+    switch (expert_path(d)) {
+        case Path::kGemv:
+            return map_err(launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, hdr, st));
+        case Path::kGrouped:
+            return map_err(launch_gateup_grouped(x, d, perm, Wgu, Wgu_s, H, hdr,
+                                                 ws_at<int4>(ws, L.tiles), st));
+        default: return MOE_ERR_UNSUPPORTED;
+    }
 }
 
 moe_status_t down_impl(const uint16_t* H, const moe_dims_t& d, const int32_t* offsets,
                        const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y, void* ws,
                        cudaStream_t st) {
-    WsHeader* hdr = ws_at<WsHeader>(ws, ws_layout(d).header);
-    if (use_gemv(d) || true)
-        return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, hdr, st));
-    return MOE_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(d);
+    WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
+    switch (expert_path(d)) {
+        case Path::kGemv:
+            return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, hdr, st));
+        case Path::kGrouped:
+            return map_err(launch_down_grouped(H, d, Wd, Wd_s, Y, hdr,
+                                               ws_at<int4>(ws, L.tiles) + L.max_tiles, st));
+        default: return MOE_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace

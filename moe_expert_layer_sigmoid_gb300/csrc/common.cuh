@@ -89,6 +89,16 @@ cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32
                              const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y,
                              WsHeader* hdr, cudaStream_t st);
 
+// Grouped tcgen05 path (prefill).  `tiles` is the tile schedule that
+// launch_descriptors wrote into the workspace (two lists of max_tiles each).
+bool grouped_supported(const moe_dims_t& d);
+cudaError_t launch_gateup_grouped(const uint16_t* x, const moe_dims_t& d, const int32_t* perm,
+                                  moe_w4_t Wgu, moe_w4_t Wgu_s, uint16_t* H, WsHeader* hdr,
+                                  const int4* tiles, cudaStream_t st);
+cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t Wd,
+                                moe_w4_t Wd_s, float* Y, WsHeader* hdr, const int4* tiles,
+                                cudaStream_t st);
+
 cudaError_t launch_combine(const float* Y, const float* topk_w, const int32_t* pos,
                            const moe_dims_t& d, uint16_t* out, cudaStream_t st);
 
