@@ -30,6 +30,8 @@ WsLayout ws_layout(const moe_dims_t& d) {
     off += align256(sizeof(float) * (size_t)(ks * T * E));
     L.tiles = off;
     off += align256(sizeof(int4) * (size_t)(2 * L.max_tiles));
+    L.xs = off;
+    off += align256(sizeof(uint16_t) * (size_t)(rows * d.d));
     L.step_bytes = off;
 
     L.topk_idx = off;
@@ -145,7 +147,8 @@ moe_status_t gateup_impl(const uint16_t* x, const moe_dims_t& d, const int32_t* 
             return map_err(launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, hdr, st));
         case Path::kGrouped:
             return map_err(launch_gateup_grouped(x, d, perm, Wgu, Wgu_s, H, hdr,
-                                                 ws_at<int4>(ws, L.tiles), st));
+                                                 ws_at<int4>(ws, L.tiles), ws_at<uint16_t>(ws, L.xs),
+                                                 st));
         default: return MOE_ERR_UNSUPPORTED;
     }
 }

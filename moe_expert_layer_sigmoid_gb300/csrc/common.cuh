@@ -44,6 +44,7 @@ struct WsLayout {
     size_t header;        // WsHeader
     size_t logits;        // fp32 [ksplit][T][E] router logit partials
     size_t tiles;         // int4 tile descriptors of the grouped kernels
+    size_t xs;            // bf16 [T*k + T][d] gathered activation rows (grouped path)
     size_t step_bytes;
     // whole-layer workspace (moe_layer_workspace_bytes) adds the intermediates
     size_t topk_idx, topk_w, counts, offsets, perm, pos, sched, H, Y, x_stage, out_stage;
@@ -92,9 +93,11 @@ cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32
 // Grouped tcgen05 path (prefill).  `tiles` is the tile schedule that
 // launch_descriptors wrote into the workspace (two lists of max_tiles each).
 bool grouped_supported(const moe_dims_t& d);
+// `xs` is workspace for the gate+up activation rows gathered into descriptor
+// order, [T*k + T][d] bf16.
 cudaError_t launch_gateup_grouped(const uint16_t* x, const moe_dims_t& d, const int32_t* perm,
                                   moe_w4_t Wgu, moe_w4_t Wgu_s, uint16_t* H, WsHeader* hdr,
-                                  const int4* tiles, cudaStream_t st);
+                                  const int4* tiles, uint16_t* xs, cudaStream_t st);
 cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t Wd,
                                 moe_w4_t Wd_s, float* Y, WsHeader* hdr, const int4* tiles,
                                 cudaStream_t st);

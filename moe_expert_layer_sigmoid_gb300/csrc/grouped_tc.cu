@@ -5,32 +5,38 @@
 // descriptors, gate and up stacked per expert, largest expert first and with
 // N-banded CTA order so CTAs that share a weight band run together and reuse
 // it in L2 (thewafflehaus/butter PR #69, commit "feat(laguna): batched prefill
-// with tensor-core projections, fused MoE, CTA scheduling"); activations are
-// read through the router-sorted token index instead of a separate gather pass
-// (thewafflehaus/FFAI PR #72, Nemotron CUTLASS MoE commit).  Their kernels are
+// with tensor-core projections, fused MoE, CTA scheduling").  Their kernels are
 // mma.sync code for GB10; this one is written for sm_103a.
 //
 // Shape of one tile: M = 128 weight rows (swap-AB: weights take the M slot),
 // N = up to 128 tokens of one expert (rounded up to 16), K = the full
-// contraction in stages of 128.  Gate+up tiles hold 64 gate rows and the 64
-// matching up rows, so SwiGLU is finished inside the tile.
+// contraction in stages of 128.  A gate+up tile holds 64 gate rows and the 64
+// matching up rows, interleaved in blocks of 16 (gate f..f+15, up f..f+15,
+// ...), so a gate row and its up row sit 16 lanes apart in the same warp and
+// SwiGLU is finished with one shuffle.
 //
-// Warp roles (14 warps, one CTA per SM):
-//   warp 0      TMA producer: per stage, the int4 weight tile (64B swizzle) and
-//               the activation rows, gathered four rows per tile::gather4 load
-//               (128B swizzle, the UMMA K-major canonical layout)
+// Activation rows are read as plain 128-row TMA boxes: the down projection
+// reads H, whose rows are already grouped by expert; gate+up reads x gathered
+// once into that same row order (gather_rows_kernel), which replaces per-row
+// gathers inside the GEMM that the TMA unit serves slowly.
+//
+// Warp roles (16 warps, one CTA per SM):
+//   warp 0      TMA producer: per tile the fp16 scale block (bulk copy), per
+//               stage the int4 weight tile (64B swizzle) and the activation
+//               tile (128B swizzle, the UMMA K-major canonical layout)
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16, A from
 //               TMEM, B from shared memory, fp32 accumulator in TMEM
-//   warps 2-5   dequantisers: int4 -> bf16 integers (exact), tcgen05.st to TMEM
-//   warps 6-13  epilogue: per quantisation group, read the group's partial
+//   warps 2-3   idle
+//   warps 4-7   dequantisers: int4 -> bf16 integers (exact), tcgen05.st to TMEM
+//   warps 8-15  epilogue: per quantisation group, read the group's partial
 //               sums from TMEM and accumulate s * partial in fp32 registers;
 //               at the end of a tile apply SwiGLU (gate+up) or store Y (down)
 //
 // Numerics: each group's partial sum is sum_k x_k * q_k with exact bf16
 // products and fp32 accumulation; multiplying by the fp16 scale s in fp32
 // gives sum_k x_k * (q_k * s), the dequantised product, without rounding the
-// weights.  TMEM: A stages at columns [0, 256), two 128-column accumulators at
-// [256, 512).
+// weights.  TMEM: two A stages at columns [0, 128), three 128-column
+// accumulators at [128, 512).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,43 +47,50 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = 14;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;
-constexpr int kKStage = 128;                    // K elements per stage
-constexpr int kTokTile = 128;                   // max tokens (N) per tile
+constexpr int kDequantWarp0 = 4;
+constexpr int kEpilogueWarp0 = 8;
+constexpr int kStages = 5;                        // shared-memory pipeline depth
+constexpr int kAStagesT = 2;                      // A operand stages in TMEM
+constexpr int kDBufs = 3;                         // accumulator buffers in TMEM
+constexpr int kKStage = 128;                      // K elements per stage
+constexpr int kTokTile = 128;                     // max tokens (N) per tile
 constexpr int kBStageBytes = 2 * kTokTile * 128;  // two 64-wide K blocks, 128 B per row
-constexpr int kAStageBytes = 128 * 64;          // 128 rows x 64 bytes of nibbles
-constexpr int kUStride = 129;                   // padded row stride of the up-row buffer (floats)
-constexpr int kMaxGroupsPerRow = 32;            // scale prefetch capacity (K / group)
+constexpr int kAStageBytes = 128 * 64;            // 128 rows x 64 bytes of nibbles
+constexpr int kMaxGroupsPerRow = 32;              // scale buffer capacity (K / group)
+constexpr int kScBytes = 128 * kMaxGroupsPerRow * 2;
 constexpr int kTmemCols = 512;
-constexpr int kTmemD = 256;                     // first accumulator column
+constexpr int kTmemD = kAStagesT * 64;            // first accumulator column
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffB = 0;
 constexpr int kOffA = kOffB + kStages * kBStageBytes;
-constexpr int kOffU = kOffA + kStages * kAStageBytes;
-constexpr int kOffSc = kOffU + 64 * kUStride * 4;
-constexpr int kOffBar = kOffSc + 2 * 128 * kMaxGroupsPerRow * 2;
-constexpr int kNumBars = 4 * kStages + 4;
+constexpr int kOffSc = kOffA + kStages * kAStageBytes;
+constexpr int kOffBar = kOffSc + 2 * kScBytes;
+// barriers: FULL[kStages], EMPTY[kStages], AREADY[2], AFREE[2], DFULL[3], DEMPTY[3], SCFULL[2], SCEMPTY[2]
+constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAReady = 2 * kStages,
+              kBarAFree = kBarAReady + kAStagesT, kBarDFull = kBarAFree + kAStagesT,
+              kBarDEmpty = kBarDFull + kDBufs, kBarScFull = kBarDEmpty + kDBufs,
+              kBarScEmpty = kBarScFull + 2, kNumBars = kBarScEmpty + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: a wait that long means something broke
 
 enum Mode : int { kGateUp = 0, kDown = 1 };
 
 struct GroupedParams {
-    CUtensorMap tm_b;       // activations (x or H), bf16, box {64, 1}, 128B swizzle
-    CUtensorMap tm_a;       // routed int4 weights, uint8 rows
-    CUtensorMap tm_a_sh;    // shared-expert int4 weights
-    const __half* s_routed; // [E * rows_per_expert][K / group]
-    const __half* s_shared; // [rows_shared][K_shared / group]
-    const int32_t* perm;
+    CUtensorMap tm_b;        // activation rows (gathered x or H), bf16, box {64, 128}, 128B swizzle
+    CUtensorMap tm_a;        // routed int4 weights, uint8 rows; gate+up box {64, 16}, down {64, 128}
+    CUtensorMap tm_a_sh;     // shared-expert int4 weights, same boxes
+    const __half* s_routed;  // [E * rows_per_expert][K / group]
+    const __half* s_shared;  // [rows_shared][K_shared / group]
     const int4* tiles;
     WsHeader* hdr;
-    void* out;              // H (bf16) or Y (fp32)
-    int64_t ld_out;         // row stride of out, elements
+    void* out;               // H (bf16) or Y (fp32)
+    int64_t ld_out;          // row stride of out, elements
     int mode;
     int T, d, k, F, Fs, group;
 };
@@ -142,12 +155,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         : "memory");
 }
 
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int y0,
-                                            int y1, int y2, int y3, uint32_t bar) {
+// Plain bulk copy global -> shared, completion counted on the mbarrier (bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
 }
 
@@ -247,16 +260,15 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* v) {
         : "memory");
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// ---------------------------------------------------------------- tile decoding
+// ---------------------------------------------------------------- tiles
 struct TileInfo {
     int grp;    // expert id, -1 for the shared expert
-    int row0;   // first row of H / Y for this tile
+    int row0;   // first row of the activation / output rows of this tile
     int n;      // tokens in the tile
     int band;   // weight band index
     int npad;   // n rounded up to 16
     int K;      // contraction length
+    int ng;     // quantisation groups along K
 };
 
 __device__ __forceinline__ TileInfo decode_tile(const GroupedParams& p, int4 t) {
@@ -267,57 +279,29 @@ __device__ __forceinline__ TileInfo decode_tile(const GroupedParams& p, int4 t) 
     ti.band = t.w;
     ti.npad = (t.z + 15) & ~15;
     ti.K = p.mode == kGateUp ? p.d : (t.x >= 0 ? p.F : p.Fs);
+    ti.ng = ti.K / p.group;
     return ti;
 }
 
-// The scales of a tile's 128 weight rows form one contiguous block (down: 128
-// rows) or two (gate+up: 64 gate rows, 64 up rows) of rows x (K / group)
-// fp16 values.  Each block starts on a 16-byte boundary (a multiple of 64 rows).
-__device__ __forceinline__ const __half* scale_block(const GroupedParams& p, const TileInfo& ti,
-                                                     int blk) {
-    const int ng = ti.K / p.group;
-    int64_t row;
+__device__ __forceinline__ int4 load_tile(const GroupedParams& p, int tile, int n_tiles) {
+    return tile < n_tiles ? __ldg(p.tiles + tile) : make_int4(0, 0, 1, 0);
+}
+
+// First weight row (within the routed or shared weight tensor) of the tile's
+// block of rows: gate+up block (gu, blk) = 16 rows; down = the 128 rows.
+__device__ __forceinline__ int weight_row(const GroupedParams& p, const TileInfo& ti, int gu,
+                                          int blk) {
     if (p.mode == kGateUp) {
         const int Fg = ti.grp >= 0 ? p.F : p.Fs;
-        const int local = blk == 0 ? 64 * ti.band : Fg + 64 * ti.band;
-        row = ti.grp >= 0 ? (int64_t)ti.grp * 2 * p.F + local : local;
-    } else {
-        const int local = 128 * ti.band;
-        row = ti.grp >= 0 ? (int64_t)ti.grp * p.d + local : local;
+        const int base = ti.grp >= 0 ? ti.grp * 2 * p.F : 0;
+        return base + gu * Fg + 64 * ti.band + 16 * blk;
     }
-    return (ti.grp >= 0 ? p.s_routed : p.s_shared) + row * ng;
-}
-
-// Loads the tile's scales as 16-byte words: word u (of 16 * ng) is returned in
-// v[u / 128] for thread t = u % 128 of the 128 loading threads.
-constexpr int kScaleWordsPerThread = kMaxGroupsPerRow * 16 / 128;  // 4
-
-__device__ __forceinline__ void load_scales(const GroupedParams& p, const TileInfo& ti, int t,
-                                            uint4* v) {
-    const int ng = ti.K / p.group;
-    const int words = 16 * ng;  // 128 rows x ng halves / 8
-    const int per_blk = p.mode == kGateUp ? 8 * ng : 16 * ng;
-#pragma unroll
-    for (int i = 0; i < kScaleWordsPerThread; ++i) {
-        const int u = t + 128 * i;
-        if (u < words) {
-            const int blk = u / per_blk, w = u - blk * per_blk;
-            v[i] = __ldg(reinterpret_cast<const uint4*>(scale_block(p, ti, blk)) + w);
-        }
-    }
-}
-
-// Stores them to shared memory as [128 rows][ng] halves.
-__device__ __forceinline__ void store_scales(__half* dst, int ng, int t, const uint4* v) {
-#pragma unroll
-    for (int i = 0; i < kScaleWordsPerThread; ++i) {
-        const int u = t + 128 * i;
-        if (u < 16 * ng) reinterpret_cast<uint4*>(dst)[u] = v[i];
-    }
+    return (ti.grp >= 0 ? ti.grp * p.d : 0) + 128 * ti.band;
 }
 
 // ---------------------------------------------------------------- the kernel
-__global__ void __launch_bounds__(kThreads, 1) grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -325,25 +309,33 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_w4a16_kernel(const __grid
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     auto bar = [&](int i) { return smem_u32(bars + i); };
-    // barrier indices
-    const int FULL = 0, EMPTY = kStages, AREADY = 2 * kStages, AFREE = 3 * kStages,
-              DFULL = 4 * kStages, DEMPTY = 4 * kStages + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(FULL + s), 1);
-            mbar_init(bar(EMPTY + s), 1 + 4);
-            mbar_init(bar(AREADY + s), 4);
-            mbar_init(bar(AFREE + s), 1);
+            mbar_init(bar(kBarFull + s), 1);
+            mbar_init(bar(kBarEmpty + s), 1 + 4);  // MMA commit + 4 dequant warps
+        }
+        for (int a = 0; a < kAStagesT; ++a) {
+            mbar_init(bar(kBarAReady + a), 4);
+            mbar_init(bar(kBarAFree + a), 1);
+        }
+        for (int b = 0; b < kDBufs; ++b) {
+            mbar_init(bar(kBarDFull + b), 1);
+            mbar_init(bar(kBarDEmpty + b), 8);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(DFULL + b), 1);
-            mbar_init(bar(DEMPTY + b), 8);
+            mbar_init(bar(kBarScFull + b), 1);
+            mbar_init(bar(kBarScEmpty + b), 8);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_a_sh)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_b)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -357,123 +349,144 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_w4a16_kernel(const __grid
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int n_tiles = *reinterpret_cast<volatile int*>(&p.hdr->n_tiles[p.mode]);
+    const int grid = gridDim.x;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        uint32_t it = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-            const TileInfo ti = decode_tile(p, __ldg(p.tiles + tile));
-            int rows[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = 4 * lane + r;
-                const int src = i < ti.n ? i : 0;
-                if (p.mode == kGateUp)
-                    rows[r] = ti.grp >= 0 ? __ldg(p.perm + ti.row0 + src) / p.k
-                                          : ti.row0 - p.T * p.k + src;
-                else
-                    rows[r] = ti.row0 + src;
-            }
-            const CUtensorMap* tma = ti.grp >= 0 ? &p.tm_a : &p.tm_a_sh;
-            int arow0, arow1 = 0;
-            if (p.mode == kGateUp) {
-                const int Fg = ti.grp >= 0 ? p.F : p.Fs;
-                const int base = ti.grp >= 0 ? ti.grp * 2 * p.F : 0;
-                arow0 = base + 64 * ti.band;
-                arow1 = base + Fg + 64 * ti.band;
-            } else {
-                arow0 = (ti.grp >= 0 ? ti.grp * p.d : 0) + 128 * ti.band;
-            }
-            const uint32_t bytes = (uint32_t)kAStageBytes + (uint32_t)ti.npad * 256u;
-            const int nks = ti.K / kKStage;
-            for (int ks = 0; ks < nks; ++ks, ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
-                if (!mbar_wait(bar(EMPTY + s), ph ^ 1, abort_flag, p.hdr)) { ok = false; break; }
-                if (lane == 0) mbar_expect_tx(bar(FULL + s), bytes);
-                __syncwarp();
-                const uint32_t bdst = sbase + kOffB + s * kBStageBytes;
-                if (4 * lane < ti.npad) {
-#pragma unroll
-                    for (int kb = 0; kb < 2; ++kb)
-                        tma_gather4(bdst + kb * (kTokTile * 128) + 4 * lane * 128, &p.tm_b,
-                                    ks * kKStage + kb * 64, rows[0], rows[1], rows[2], rows[3],
-                                    bar(FULL + s));
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            int tc = 0;
+            int4 cur = load_tile(p, blockIdx.x, n_tiles);
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid, ++tc) {
+                const int4 nxt = load_tile(p, tile + grid, n_tiles);  // one tile ahead
+                const TileInfo ti = decode_tile(p, cur);
+                // the tile's scale block(s)
+                const int sb = tc & 1;
+                if (!mbar_wait(bar(kBarScEmpty + sb), ((tc >> 1) & 1) ^ 1, abort_flag, p.hdr)) {
+                    ok = false;
+                    break;
                 }
-                if (lane == 0) {
+                const __half* sbase_g = ti.grp >= 0 ? p.s_routed : p.s_shared;
+                const uint32_t scdst = sbase + kOffSc + sb * kScBytes;
+                if (p.mode == kGateUp) {
+                    const uint32_t blk_bytes = 64u * ti.ng * 2u;
+                    mbar_expect_tx(bar(kBarScFull + sb), 2 * blk_bytes);
+                    bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, blk_bytes,
+                              bar(kBarScFull + sb));
+                    bulk_load(scdst + blk_bytes, sbase_g + (int64_t)weight_row(p, ti, 1, 0) * ti.ng,
+                              blk_bytes, bar(kBarScFull + sb));
+                } else {
+                    const uint32_t bytes = 128u * ti.ng * 2u;
+                    mbar_expect_tx(bar(kBarScFull + sb), bytes);
+                    bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, bytes,
+                              bar(kBarScFull + sb));
+                }
+                const CUtensorMap* tma = ti.grp >= 0 ? &p.tm_a : &p.tm_a_sh;
+                const int nks = ti.K / kKStage;
+                for (int ks = 0; ks < nks; ++ks, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1, abort_flag, p.hdr)) { ok = false; break; }
+                    mbar_expect_tx(bar(kBarFull + s), (uint32_t)(kAStageBytes + kBStageBytes));
                     const uint32_t adst = sbase + kOffA + s * kAStageBytes;
-                    tma_load_2d(adst, tma, ks * 64, arow0, bar(FULL + s));
-                    if (p.mode == kGateUp) tma_load_2d(adst + 64 * 64, tma, ks * 64, arow1, bar(FULL + s));
+                    if (p.mode == kGateUp) {
+                        // rows m = 32*blk + 16*gu + i: gate and up blocks of 16 interleaved
+#pragma unroll
+                        for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+                            for (int gu = 0; gu < 2; ++gu)
+                                tma_load_2d(adst + (32 * blk + 16 * gu) * 64, tma, ks * 64,
+                                            weight_row(p, ti, gu, blk), bar(kBarFull + s));
+                    } else {
+                        tma_load_2d(adst, tma, ks * 64, weight_row(p, ti, 0, 0), bar(kBarFull + s));
+                    }
+                    const uint32_t bdst = sbase + kOffB + s * kBStageBytes;
+                    tma_load_2d(bdst, &p.tm_b, ks * kKStage, ti.row0, bar(kBarFull + s));
+                    tma_load_2d(bdst + kTokTile * 128, &p.tm_b, ks * kKStage + 64, ti.row0,
+                                bar(kBarFull + s));
                 }
+                cur = nxt;
             }
+            // do not leave with copies in flight
+            if (!ok)
+                for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j)
+                    mbar_wait(bar(kBarFull + j % kStages), (j / kStages) & 1, abort_flag, p.hdr);
         }
-        // do not leave with copies in flight: wait until every issued stage has landed
-        if (!ok) {
-            for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j)
-                mbar_wait(bar(FULL + j % kStages), (j / kStages) & 1, abort_flag, p.hdr);
-        }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t it = 0, gi = 0;
             bool ok = true;
             const int kk_per_group = p.group / 16;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const TileInfo ti = decode_tile(p, __ldg(p.tiles + tile));
+            int4 cur = load_tile(p, blockIdx.x, n_tiles);
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
+                const int4 nxt = load_tile(p, tile + grid, n_tiles);
+                const TileInfo ti = decode_tile(p, cur);
                 const uint32_t idesc = idesc_bf16(128, ti.npad);
                 const int nks = ti.K / kKStage;
                 for (int ks = 0; ks < nks && ok; ++ks, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
-                    if (!mbar_wait(bar(FULL + s), ph, abort_flag, p.hdr) ||
-                        !mbar_wait(bar(AREADY + s), ph, abort_flag, p.hdr)) { ok = false; break; }
+                    const int ta = it % kAStagesT;
+                    const uint32_t tph = (it / kAStagesT) & 1;
+                    if (!mbar_wait(bar(kBarFull + s), ph, abort_flag, p.hdr) ||
+                        !mbar_wait(bar(kBarAReady + ta), tph, abort_flag, p.hdr)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t bstage = sbase + kOffB + s * kBStageBytes;
                     for (int gg = 0; gg < kKStage / p.group; ++gg, ++gi) {
-                        const int b = gi & 1;
-                        if (!mbar_wait(bar(DEMPTY + b), ((gi >> 1) & 1) ^ 1, abort_flag, p.hdr)) { ok = false; break; }
+                        const int b = gi % kDBufs;
+                        if (!mbar_wait(bar(kBarDEmpty + b), ((gi / kDBufs) & 1) ^ 1, abort_flag, p.hdr)) {
+                            ok = false;
+                            break;
+                        }
                         tc_fence_after();
                         for (int kk = 0; kk < kk_per_group; ++kk) {
                             const int kg = gg * kk_per_group + kk;  // 16-wide K step within the stage
-                            const uint32_t a_addr = tmem + (uint32_t)(s * 64 + kg * 8);
-                            const uint64_t bdesc =
-                                smem_desc_sw128(bstage + (kg >> 2) * (kTokTile * 128) + (kg & 3) * 32);
+                            const uint32_t a_addr = tmem + (uint32_t)(ta * 64 + kg * 8);
+                            const uint64_t bdesc = smem_desc_sw128(bstage + (kg >> 2) * (kTokTile * 128) +
+                                                                   (kg & 3) * 32);
                             mma_ts(tmem + kTmemD + b * 128, a_addr, bdesc, idesc, kk > 0 ? 1u : 0u);
                         }
-                        mma_commit(bar(DFULL + b));
+                        mma_commit(bar(kBarDFull + b));
                     }
                     if (!ok) break;
-                    mma_commit(bar(EMPTY + s));
-                    mma_commit(bar(AFREE + s));
+                    mma_commit(bar(kBarEmpty + s));
+                    mma_commit(bar(kBarAFree + ta));
                 }
+                cur = nxt;
             }
             // the last commit has landed before the CTA can exit
             if (ok && it > 0)
-                mbar_wait(bar(AFREE + (it - 1) % kStages), ((it - 1) / kStages) & 1, abort_flag, p.hdr);
+                mbar_wait(bar(kBarAFree + (it - 1) % kAStagesT), ((it - 1) / kAStagesT) & 1, abort_flag,
+                          p.hdr);
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp >= kDequantWarp0 && warp < kEpilogueWarp0) {
         // ------------------------------------------------------------ dequantisers
         const int q = warp & 3;
         const int m = q * 32 + lane;  // tile row = TMEM lane
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-            const TileInfo ti = decode_tile(p, __ldg(p.tiles + tile));
+        int4 cur = load_tile(p, blockIdx.x, n_tiles);
+        for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
+            const int4 nxt = load_tile(p, tile + grid, n_tiles);
+            const TileInfo ti = decode_tile(p, cur);
             const int nks = ti.K / kKStage;
             for (int ks = 0; ks < nks; ++ks, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
-                if (!mbar_wait(bar(FULL + s), ph, abort_flag, p.hdr)) { ok = false; break; }
+                if (!mbar_wait(bar(kBarFull + s), ph, abort_flag, p.hdr)) { ok = false; break; }
+                // row m of the int4 tile: 64 bytes, 16-byte chunks 64B-swizzled by the TMA
                 const uint8_t* arow = smem + kOffA + s * kAStageBytes + m * 64;
                 uint4 v[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     v[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ ((m >> 1) & 3)) << 4));
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(EMPTY + s));
+                if (lane == 0) mbar_arrive(bar(kBarEmpty + s));
                 uint32_t r[64];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -482,89 +495,87 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_w4a16_kernel(const __grid
                     nib8_to_bf16x2(v[c].z, r + 16 * c + 8);
                     nib8_to_bf16x2(v[c].w, r + 16 * c + 12);
                 }
-                if (!mbar_wait(bar(AFREE + s), ph ^ 1, abort_flag, p.hdr)) { ok = false; break; }
+                const int ta = it % kAStagesT;
+                if (!mbar_wait(bar(kBarAFree + ta), ((it / kAStagesT) & 1) ^ 1, abort_flag, p.hdr)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                tmem_st_x64(tmem + lane_base + (uint32_t)(s * 64), r);
+                tmem_st_x64(tmem + lane_base + (uint32_t)(ta * 64), r);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(AREADY + s));
+                if (lane == 0) mbar_arrive(bar(kBarAReady + ta));
             }
+            cur = nxt;
         }
-    } else {
+    } else if (warp >= kEpilogueWarp0) {
         // ------------------------------------------------------------ epilogue
         // After a failed wait every epilogue warp keeps walking the same tiles
-        // (skipping the work) so the named barriers stay matched.
+        // (skipping the work), so no warp waits on a barrier the others left.
         const int q = warp & 3;
-        const int half = (warp - 6) >> 2;
+        const int half = (warp - kEpilogueWarp0) >> 2;
         const int m = q * 32 + lane;
         const int col0 = half * 64;
-        const int t128 = threadIdx.x - 6 * 32 - half * 128;  // 0..127 within the half
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        __half* sc = reinterpret_cast<__half*>(smem + kOffSc);  // [2][128 * kMaxGroupsPerRow]
-        float* U = reinterpret_cast<float*>(smem + kOffU);        // [64][kUStride]
+        // gate+up: row m is gate (gu = 0) or up (gu = 1) row f_local of the band
+        const int gu = (m >> 4) & 1;
+        const int f_local = (m >> 5) * 16 + (m & 15);
         uint32_t gi = 0;
         bool ok = true;
-        int tile = blockIdx.x;
-        if (tile < n_tiles && half == 0) {  // scales of the first tile
-            const TileInfo ti = decode_tile(p, __ldg(p.tiles + tile));
-            uint4 v[kScaleWordsPerThread];
-            load_scales(p, ti, t128, v);
-            store_scales(sc, ti.K / p.group, t128, v);
-        }
-        epi_bar();
-        for (int tc = 0; tile < n_tiles; tile += gridDim.x, ++tc) {
-            const TileInfo ti = decode_tile(p, __ldg(p.tiles + tile));
-            const int ngroups = ti.K / p.group;
-            const __half* scur = sc + (tc & 1) * 128 * kMaxGroupsPerRow + m * ngroups;
-            // prefetch the next tile's scales into registers
-            uint4 nxt[kScaleWordsPerThread];
-            const int next = tile + gridDim.x;
-            TileInfo tn = ti;
-            if (next < n_tiles) tn = decode_tile(p, __ldg(p.tiles + next));
-            if (next < n_tiles && half == 0) load_scales(p, tn, t128, nxt);
+        int tc = 0;
+        int4 cur = load_tile(p, blockIdx.x, n_tiles);
+        for (int tile = blockIdx.x; tile < n_tiles; tile += grid, ++tc) {
+            const int4 nxt = load_tile(p, tile + grid, n_tiles);
+            const TileInfo ti = decode_tile(p, cur);
+            const int sb = tc & 1;
+            if (ok && !mbar_wait(bar(kBarScFull + sb), (tc >> 1) & 1, abort_flag, p.hdr)) ok = false;
+            const __half* sc = reinterpret_cast<const __half*>(smem + kOffSc + sb * kScBytes);
+            const __half* srow = p.mode == kGateUp ? sc + (gu * 64 + f_local) * ti.ng : sc + m * ti.ng;
             float acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.f;
-            for (int g = 0; g < ngroups; ++g, ++gi) {
-                const int b = gi & 1;
-                if (ok && !mbar_wait(bar(DFULL + b), (gi >> 1) & 1, abort_flag, p.hdr)) ok = false;
+            for (int g = 0; g < ti.ng; ++g, ++gi) {
+                const int b = gi % kDBufs;
+                if (ok && !mbar_wait(bar(kBarDFull + b), (gi / kDBufs) & 1, abort_flag, p.hdr)) ok = false;
                 if (!ok) continue;
                 tc_fence_after();
-                const float s = __half2float(scur[g]);
+                const float s = __half2float(srow[g]);
                 const uint32_t dcol = tmem + lane_base + (uint32_t)(kTmemD + b * 128 + col0);
+                if (col0 < ti.npad) {
+                    uint32_t v[32];
+                    tmem_ld_x32(dcol, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    if (col0 + 32 * c < ti.npad) {
-                        uint32_t v[32];
-                        tmem_ld_x32(dcol + 32 * c, v);
-                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    for (int j = 0; j < 32; ++j) acc[j] = fmaf(s, __uint_as_float(v[j]), acc[j]);
+                }
+                if (col0 + 32 < ti.npad) {
+                    uint32_t v[32];
+                    tmem_ld_x32(dcol + 32, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[32 * c + j] = fmaf(s, __uint_as_float(v[j]), acc[32 * c + j]);
-                    }
+                    for (int j = 0; j < 32; ++j) acc[32 + j] = fmaf(s, __uint_as_float(v[j]), acc[32 + j]);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(DEMPTY + b));
+                if (lane == 0) mbar_arrive(bar(kBarDEmpty + b));
             }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(bar(kBarScEmpty + sb));
             if (p.mode == kGateUp) {
-                if (ok && m >= 64) {
+                // lane i holds gate row f, lane i ^ 16 the up row of the same f
+                uint16_t* H = reinterpret_cast<uint16_t*>(p.out);
+                const int f = 64 * ti.band + f_local;
+                const bool lo = (lane & 16) == 0;
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) U[(m - 64) * kUStride + col0 + j] = acc[j];
-                }
-                epi_bar();
-                if (ok && m < 64) {
-                    uint16_t* H = reinterpret_cast<uint16_t*>(p.out);
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        const int nn = col0 + j;
-                        if (nn < ti.n) {
-                            const float gv = acc[j];
-                            const float uv = U[m * kUStride + nn];
-                            const float h = gv / (1.0f + expf(-gv)) * uv;
-                            H[(int64_t)(ti.row0 + nn) * p.ld_out + 64 * ti.band + m] = float_to_bf16_bits(h);
-                        }
+                for (int j = 0; j < 64; ++j) {
+                    const float other = __shfl_xor_sync(0xffffffffu, acc[j], 16);
+                    const float gv = lo ? acc[j] : other;
+                    const float uv = lo ? other : acc[j];
+                    const int nn = col0 + j;
+                    if (ok && lo == (j < 32) && nn < ti.n) {
+                        const float h = gv / (1.0f + expf(-gv)) * uv;
+                        H[(int64_t)(ti.row0 + nn) * p.ld_out + f] = float_to_bf16_bits(h);
                     }
                 }
             } else if (ok) {
@@ -575,11 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_w4a16_kernel(const __grid
                     if (nn < ti.n) Y[(int64_t)(ti.row0 + nn) * p.ld_out + 128 * ti.band + m] = acc[j];
                 }
             }
-            // publish the next tile's scales: the other buffer is free, every
-            // epilogue thread has finished the previous tile
-            if (next < n_tiles && half == 0)
-                store_scales(sc + ((tc + 1) & 1) * 128 * kMaxGroupsPerRow, tn.K / p.group, t128, nxt);
-            epi_bar();
+            cur = nxt;
         }
     }
 
@@ -591,6 +598,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_w4a16_kernel(const __grid
                      "r"(kTmemCols)
                      : "memory");
     }
+}
+
+// Gate+up activation rows in descriptor order: xs[r] = x[perm[r] / k] for the
+// T*k routed rows, then xs[T*k + t] = x[t] for the shared expert.  One warp
+// per row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ perm, int T,
+                                                          int k, int d, uint16_t* __restrict__ xs) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t slots = (int64_t)T * k;
+    if (r >= slots + T) return;
+    const int64_t t = r < slots ? __ldg(perm + r) / k : r - slots;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
+    uint4* dst = reinterpret_cast<uint4*>(xs + r * d);
+    for (int c = threadIdx.x & 31; c < d / 8; c += 32) dst[c] = __ldg(src + c);
 }
 
 // ---------------------------------------------------------------- host side
@@ -608,6 +630,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// 2D row-major tensor [outer][inner] with rows row_bytes apart.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
               CUtensorMapSwizzle sw) {
@@ -646,26 +669,28 @@ bool grouped_supported(const moe_dims_t& d) {
     const int Fmax = std::max(d.F, d.F_s);
     return d.d % kKStage == 0 && d.F % kKStage == 0 && d.F_s % kKStage == 0 &&
            d.d / d.group <= kMaxGroupsPerRow && Fmax / d.group <= kMaxGroupsPerRow &&
-           d.F % 64 == 0 && d.F_s % 64 == 0 && d.d % 128 == 0 && d.group % 16 == 0 &&
-           kKStage % d.group == 0;
+           d.F % 64 == 0 && d.F_s % 64 == 0 && d.group % 16 == 0 && kKStage % d.group == 0;
 }
 
 cudaError_t launch_gateup_grouped(const uint16_t* x, const moe_dims_t& d, const int32_t* perm,
                                   moe_w4_t Wgu, moe_w4_t Wgu_s, uint16_t* H, WsHeader* hdr,
-                                  const int4* tiles, cudaStream_t st) {
+                                  const int4* tiles, uint16_t* xs, cudaStream_t st) {
+    const int64_t rows = (int64_t)d.T * d.k + d.T;
+    gather_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(x, perm, d.T, d.k, d.d, xs);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
     GroupedParams prm;
     memset(&prm, 0, sizeof(prm));
     const int Fmax = std::max(d.F, d.F_s);
-    if (!make_map(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, d.d, d.T, (uint64_t)d.d * 2, 64, 1,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!make_map(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs, d.d, rows, (uint64_t)d.d * 2, 64,
+                  kTokTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&prm.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wgu.q, d.d / 2, (uint64_t)d.E * 2 * d.F,
-                  d.d / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+                  d.d / 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&prm.tm_a_sh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wgu_s.q, d.d / 2,
-                  (uint64_t)2 * d.F_s, d.d / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+                  (uint64_t)2 * d.F_s, d.d / 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     prm.s_routed = reinterpret_cast<const __half*>(Wgu.s);
     prm.s_shared = reinterpret_cast<const __half*>(Wgu_s.s);
-    prm.perm = perm;
     prm.tiles = tiles;
     prm.hdr = hdr;
     prm.out = H;
@@ -682,8 +707,8 @@ cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t
     memset(&prm, 0, sizeof(prm));
     const int Fmax = std::max(d.F, d.F_s);
     const uint64_t rows = (uint64_t)d.T * d.k + d.T;
-    if (!make_map(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Fmax, rows, (uint64_t)Fmax * 2, 64, 1,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!make_map(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Fmax, rows, (uint64_t)Fmax * 2, 64,
+                  kTokTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&prm.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wd.q, d.F / 2, (uint64_t)d.E * d.d,
                   d.F / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&prm.tm_a_sh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wd_s.q, d.F_s / 2, (uint64_t)d.d,
@@ -691,7 +716,6 @@ cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t
         return cudaErrorInvalidValue;
     prm.s_routed = reinterpret_cast<const __half*>(Wd.s);
     prm.s_shared = reinterpret_cast<const __half*>(Wd_s.s);
-    prm.perm = nullptr;
     prm.tiles = tiles;
     prm.hdr = hdr;
     prm.out = Y;
