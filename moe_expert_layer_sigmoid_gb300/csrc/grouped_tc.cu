@@ -52,8 +52,9 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kDequantWarp0 = 4;
 constexpr int kEpilogueWarp0 = 8;
 constexpr int kStages = 5;                        // shared-memory pipeline depth
-constexpr int kAStagesT = 2;                      // A operand stages in TMEM
-constexpr int kDBufs = 3;                         // accumulator buffers in TMEM
+constexpr int kAStagesT = 4;                      // A operand stages in TMEM
+constexpr int kDBufs = 2;                         // accumulator buffers in TMEM
+static_assert(kAStagesT < kStages, "dequant reuses the stage barrier of the MMA it waits for");
 constexpr int kKStage = 128;                      // K elements per stage
 constexpr int kTokTile = 128;                     // max tokens (N) per tile
 constexpr int kBStageBytes = 2 * kTokTile * 128;  // two 64-wide K blocks, 128 B per row
@@ -68,9 +69,12 @@ constexpr int kOffB = 0;
 constexpr int kOffA = kOffB + kStages * kBStageBytes;
 constexpr int kOffSc = kOffA + kStages * kAStageBytes;
 constexpr int kOffBar = kOffSc + 2 * kScBytes;
-// barriers: FULL[kStages], EMPTY[kStages], AREADY[2], AFREE[2], DFULL[3], DEMPTY[3], SCFULL[2], SCEMPTY[2]
+// barriers: FULL[kStages], EMPTY[kStages], AREADY[kAStagesT], DFULL[2], DEMPTY[2], SCFULL[2], SCEMPTY[2]
+// EMPTY[s] completes when the MMAs of smem stage s are done and the dequant
+// warps have read its int4 tile; it also tells the dequant warps that the
+// TMEM A stage those MMAs read is free again.
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAReady = 2 * kStages,
-              kBarAFree = kBarAReady + kAStagesT, kBarDFull = kBarAFree + kAStagesT,
+              kBarDFull = kBarAReady + kAStagesT,
               kBarDEmpty = kBarDFull + kDBufs, kBarScFull = kBarDEmpty + kDBufs,
               kBarScEmpty = kBarScFull + 2, kNumBars = kBarScEmpty + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -119,7 +123,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -152,6 +156,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            int c2, int c3, int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
         : "memory");
 }
 
@@ -271,6 +293,7 @@ struct TileInfo {
     int ng;     // quantisation groups along K
 };
 
+template <int G>
 __device__ __forceinline__ TileInfo decode_tile(const GroupedParams& p, int4 t) {
     TileInfo ti;
     ti.grp = t.x;
@@ -279,7 +302,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GroupedParams& p, int4 t) 
     ti.band = t.w;
     ti.npad = (t.z + 15) & ~15;
     ti.K = p.mode == kGateUp ? p.d : (t.x >= 0 ? p.F : p.Fs);
-    ti.ng = ti.K / p.group;
+    ti.ng = ti.K / G;
     return ti;
 }
 
@@ -300,6 +323,7 @@ __device__ __forceinline__ int weight_row(const GroupedParams& p, const TileInfo
 }
 
 // ---------------------------------------------------------------- the kernel
+template <int G>  // quantisation group size along K
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -317,10 +341,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
             mbar_init(bar(kBarFull + s), 1);
             mbar_init(bar(kBarEmpty + s), 1 + 4);  // MMA commit + 4 dequant warps
         }
-        for (int a = 0; a < kAStagesT; ++a) {
-            mbar_init(bar(kBarAReady + a), 4);
-            mbar_init(bar(kBarAFree + a), 1);
-        }
+        for (int a = 0; a < kAStagesT; ++a) mbar_init(bar(kBarAReady + a), 4);
         for (int b = 0; b < kDBufs; ++b) {
             mbar_init(bar(kBarDFull + b), 1);
             mbar_init(bar(kBarDEmpty + b), 8);
@@ -360,7 +381,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
             int4 cur = load_tile(p, blockIdx.x, n_tiles);
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid, ++tc) {
                 const int4 nxt = load_tile(p, tile + grid, n_tiles);  // one tile ahead
-                const TileInfo ti = decode_tile(p, cur);
+                const TileInfo ti = decode_tile<G>(p, cur);
                 // the tile's scale block(s)
                 const int sb = tc & 1;
                 if (!mbar_wait(bar(kBarScEmpty + sb), ((tc >> 1) & 1) ^ 1, abort_flag, p.hdr)) {
@@ -389,21 +410,14 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     const uint32_t ph = (it / kStages) & 1;
                     if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1, abort_flag, p.hdr)) { ok = false; break; }
                     mbar_expect_tx(bar(kBarFull + s), (uint32_t)(kAStageBytes + kBStageBytes));
+                    // one box each: the weight tile and both 64-wide K blocks of the activations
                     const uint32_t adst = sbase + kOffA + s * kAStageBytes;
-                    if (p.mode == kGateUp) {
-                        // rows m = 32*blk + 16*gu + i: gate and up blocks of 16 interleaved
-#pragma unroll
-                        for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-                            for (int gu = 0; gu < 2; ++gu)
-                                tma_load_2d(adst + (32 * blk + 16 * gu) * 64, tma, ks * 64,
-                                            weight_row(p, ti, gu, blk), bar(kBarFull + s));
-                    } else {
+                    if (p.mode == kGateUp)  // rows m = 32*blk + 16*gu + i (gate/up interleaved)
+                        tma_load_5d(adst, tma, ks * 64, 0, 0, 4 * ti.band, ti.grp >= 0 ? ti.grp : 0,
+                                    bar(kBarFull + s));
+                    else
                         tma_load_2d(adst, tma, ks * 64, weight_row(p, ti, 0, 0), bar(kBarFull + s));
-                    }
-                    const uint32_t bdst = sbase + kOffB + s * kBStageBytes;
-                    tma_load_2d(bdst, &p.tm_b, ks * kKStage, ti.row0, bar(kBarFull + s));
-                    tma_load_2d(bdst + kTokTile * 128, &p.tm_b, ks * kKStage + 64, ti.row0,
+                    tma_load_3d(sbase + kOffB + s * kBStageBytes, &p.tm_b, 0, ti.row0, 2 * ks,
                                 bar(kBarFull + s));
                 }
                 cur = nxt;
@@ -419,11 +433,10 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         if (lane == 0) {
             uint32_t it = 0, gi = 0;
             bool ok = true;
-            const int kk_per_group = p.group / 16;
             int4 cur = load_tile(p, blockIdx.x, n_tiles);
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
                 const int4 nxt = load_tile(p, tile + grid, n_tiles);
-                const TileInfo ti = decode_tile(p, cur);
+                const TileInfo ti = decode_tile<G>(p, cur);
                 const uint32_t idesc = idesc_bf16(128, ti.npad);
                 const int nks = ti.K / kKStage;
                 for (int ks = 0; ks < nks && ok; ++ks, ++it) {
@@ -434,33 +447,36 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     if (!mbar_wait(bar(kBarFull + s), ph, abort_flag, p.hdr) ||
                         !mbar_wait(bar(kBarAReady + ta), tph, abort_flag, p.hdr)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t bstage = sbase + kOffB + s * kBStageBytes;
-                    for (int gg = 0; gg < kKStage / p.group; ++gg, ++gi) {
-                        const int b = gi % kDBufs;
-                        if (!mbar_wait(bar(kBarDEmpty + b), ((gi / kDBufs) & 1) ^ 1, abort_flag, p.hdr)) {
+                    // descriptor of the stage's B tile; K steps add (kg/4)*16 KB + (kg%4)*32 B,
+                    // i.e. (kg/4)*1024 + (kg%4)*2 in the 16-byte address field
+                    const uint64_t bdesc0 = smem_desc_sw128(sbase + kOffB + s * kBStageBytes);
+                    const uint32_t a0 = tmem + (uint32_t)(ta * 64);
+#pragma unroll
+                    for (int gg = 0; gg < kKStage / G; ++gg, ++gi) {
+                        const int b = gi & 1;
+                        if (!mbar_wait(bar(kBarDEmpty + b), ((gi >> 1) & 1) ^ 1, abort_flag, p.hdr)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        for (int kk = 0; kk < kk_per_group; ++kk) {
-                            const int kg = gg * kk_per_group + kk;  // 16-wide K step within the stage
-                            const uint32_t a_addr = tmem + (uint32_t)(ta * 64 + kg * 8);
-                            const uint64_t bdesc = smem_desc_sw128(bstage + (kg >> 2) * (kTokTile * 128) +
-                                                                   (kg & 3) * 32);
-                            mma_ts(tmem + kTmemD + b * 128, a_addr, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        const uint32_t dcol = tmem + (uint32_t)(kTmemD + b * 128);
+#pragma unroll
+                        for (int kk = 0; kk < G / 16; ++kk) {
+                            const int kg = gg * (G / 16) + kk;  // 16-wide K step within the stage
+                            mma_ts(dcol, a0 + (uint32_t)(kg * 8),
+                                   bdesc0 + (uint64_t)((kg >> 2) * 1024 + (kg & 3) * 2), idesc,
+                                   kk > 0 ? 1u : 0u);
                         }
                         mma_commit(bar(kBarDFull + b));
                     }
                     if (!ok) break;
                     mma_commit(bar(kBarEmpty + s));
-                    mma_commit(bar(kBarAFree + ta));
                 }
                 cur = nxt;
             }
             // the last commit has landed before the CTA can exit
             if (ok && it > 0)
-                mbar_wait(bar(kBarAFree + (it - 1) % kAStagesT), ((it - 1) / kAStagesT) & 1, abort_flag,
-                          p.hdr);
+                mbar_wait(bar(kBarEmpty + (it - 1) % kStages), ((it - 1) / kStages) & 1, abort_flag, p.hdr);
         }
         __syncwarp();
     } else if (warp >= kDequantWarp0 && warp < kEpilogueWarp0) {
@@ -473,7 +489,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         int4 cur = load_tile(p, blockIdx.x, n_tiles);
         for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
             const int4 nxt = load_tile(p, tile + grid, n_tiles);
-            const TileInfo ti = decode_tile(p, cur);
+            const TileInfo ti = decode_tile<G>(p, cur);
             const int nks = ti.K / kKStage;
             for (int ks = 0; ks < nks; ++ks, ++it) {
                 const int s = it % kStages;
@@ -496,9 +512,12 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     nib8_to_bf16x2(v[c].w, r + 16 * c + 12);
                 }
                 const int ta = it % kAStagesT;
-                if (!mbar_wait(bar(kBarAFree + ta), ((it / kAStagesT) & 1) ^ 1, abort_flag, p.hdr)) {
-                    ok = false;
-                    break;
+                if (it >= kAStagesT) {  // TMEM stage ta is free once the MMAs of stage it - kAStagesT are done
+                    const uint32_t j = it - kAStagesT;
+                    if (!mbar_wait(bar(kBarEmpty + j % kStages), (j / kStages) & 1, abort_flag, p.hdr)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 tc_fence_after();
                 tmem_st_x64(tmem + lane_base + (uint32_t)(ta * 64), r);
@@ -527,7 +546,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         int4 cur = load_tile(p, blockIdx.x, n_tiles);
         for (int tile = blockIdx.x; tile < n_tiles; tile += grid, ++tc) {
             const int4 nxt = load_tile(p, tile + grid, n_tiles);
-            const TileInfo ti = decode_tile(p, cur);
+            const TileInfo ti = decode_tile<G>(p, cur);
             const int sb = tc & 1;
             if (ok && !mbar_wait(bar(kBarScFull + sb), (tc >> 1) & 1, abort_flag, p.hdr)) ok = false;
             const __half* sc = reinterpret_cast<const __half*>(smem + kOffSc + sb * kScBytes);
@@ -536,8 +555,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.f;
             for (int g = 0; g < ti.ng; ++g, ++gi) {
-                const int b = gi % kDBufs;
-                if (ok && !mbar_wait(bar(kBarDFull + b), (gi / kDBufs) & 1, abort_flag, p.hdr)) ok = false;
+                const int b = gi & 1;
+                if (ok && !mbar_wait(bar(kBarDFull + b), (gi >> 1) & 1, abort_flag, p.hdr)) ok = false;
                 if (!ok) continue;
                 tc_fence_after();
                 const float s = __half2float(srow[g]);
@@ -630,6 +649,41 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// General tiled map (rank <= 5); strides[i] is the byte stride of dim i + 1.
+bool make_map_nd(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank,
+                 const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                 CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Activation rows [rows][cols] bf16 read as {64 elements, 128 rows, 2 K blocks}:
+// one box fills both 64-wide K blocks of a stage.
+bool make_act_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+    const cuuint64_t dims[3] = {64, rows, cols / 64};
+    const cuuint64_t strides[2] = {cols * 2, 128};
+    const cuuint32_t box[3] = {64, kTokTile, 2};
+    return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 3, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Gate+up int4 weights of `experts` experts ([experts][2Fg][d/2] bytes) read as
+// {64 bytes of K, 16 rows, gate/up, 16-row blocks, expert}: one box holds 64
+// gate rows and their 64 up rows interleaved in blocks of 16.
+bool make_gateup_map(CUtensorMap* m, const void* base, uint64_t d, uint64_t Fg, uint64_t experts) {
+    const uint64_t rb = d / 2;
+    const cuuint64_t dims[5] = {rb, 16, 2, Fg / 16, experts};
+    const cuuint64_t strides[4] = {rb, Fg * rb, 16 * rb, 2 * Fg * rb};
+    const cuuint32_t box[5] = {64, 16, 2, 4, 1};
+    return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 5, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 // 2D row-major tensor [outer][inner] with rows row_bytes apart.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
@@ -654,13 +708,23 @@ int sm_count() {
     return counts[dev];
 }
 
-cudaError_t launch(GroupedParams& prm, cudaStream_t st) {
-    cudaError_t err = ensure_dynamic_smem((const void*)grouped_w4a16_kernel, kSmemBytes);
+template <int G>
+cudaError_t launch_g(GroupedParams& prm, int sms, cudaStream_t st) {
+    cudaError_t err = ensure_dynamic_smem((const void*)grouped_w4a16_kernel<G>, kSmemBytes);
     if (err != cudaSuccess) return err;
+    grouped_w4a16_kernel<G><<<sms, kThreads, kSmemBytes, st>>>(prm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch(GroupedParams& prm, cudaStream_t st) {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    grouped_w4a16_kernel<<<sms, kThreads, kSmemBytes, st>>>(prm);
-    return cudaGetLastError();
+    switch (prm.group) {
+        case 32: return launch_g<32>(prm, sms, st);
+        case 64: return launch_g<64>(prm, sms, st);
+        case 128: return launch_g<128>(prm, sms, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -682,12 +746,9 @@ cudaError_t launch_gateup_grouped(const uint16_t* x, const moe_dims_t& d, const 
     GroupedParams prm;
     memset(&prm, 0, sizeof(prm));
     const int Fmax = std::max(d.F, d.F_s);
-    if (!make_map(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs, d.d, rows, (uint64_t)d.d * 2, 64,
-                  kTokTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&prm.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wgu.q, d.d / 2, (uint64_t)d.E * 2 * d.F,
-                  d.d / 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&prm.tm_a_sh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wgu_s.q, d.d / 2,
-                  (uint64_t)2 * d.F_s, d.d / 2, 64, 16, CU_TENSOR_MAP_SWIZZLE_64B))
+    if (!make_act_map(&prm.tm_b, xs, d.d, rows) ||
+        !make_gateup_map(&prm.tm_a, Wgu.q, d.d, d.F, d.E) ||
+        !make_gateup_map(&prm.tm_a_sh, Wgu_s.q, d.d, d.F_s, 1))
         return cudaErrorInvalidValue;
     prm.s_routed = reinterpret_cast<const __half*>(Wgu.s);
     prm.s_shared = reinterpret_cast<const __half*>(Wgu_s.s);
@@ -707,8 +768,7 @@ cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t
     memset(&prm, 0, sizeof(prm));
     const int Fmax = std::max(d.F, d.F_s);
     const uint64_t rows = (uint64_t)d.T * d.k + d.T;
-    if (!make_map(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, H, Fmax, rows, (uint64_t)Fmax * 2, 64,
-                  kTokTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!make_act_map(&prm.tm_b, H, Fmax, rows) ||
         !make_map(&prm.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wd.q, d.F / 2, (uint64_t)d.E * d.d,
                   d.F / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&prm.tm_a_sh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wd_s.q, d.F_s / 2, (uint64_t)d.d,
