@@ -112,11 +112,12 @@ class ClockSampler:
 
 def kernels_per_step(cfg, flags=0):
     """Kernels libmoe.so launches for one moe_layer_forward (memset nodes excluded)."""
-    router = 2
-    desc = 2
-    experts = 2
-    combine = 1
-    return router + desc + experts + combine
+    gemv = (flags & 0x1) or (cfg.T <= 64 and not flags & 0x2)
+    if gemv and cfg.T <= 64:
+        return 3  # fused router + descriptors, gate+up GEMV, down GEMV + combine
+    if gemv:
+        return 2 + 2 + 2  # router (2), descriptors (2), the two GEMVs (combine fused)
+    return 2 + 2 + 1 + 2 + 1  # router, descriptors, row gather, two grouped GEMMs, combine
 
 
 class GpuBench:
@@ -154,6 +155,8 @@ class GpuBench:
                                    self.ws, stream=stream)
 
     def capture(self):
+        """One graph per slot, and one graph of all slots in a row (so that a
+        replay is launched per nslots steps, not per step)."""
         torch = self.torch
         self.graphs = []
         with torch.cuda.stream(self.stream):
@@ -165,19 +168,30 @@ class GpuBench:
             with torch.cuda.graph(g, stream=self.stream):
                 self.step(i, self.stream)
             self.graphs.append(g)
+        self.round = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.round, stream=self.stream):
+            for i in range(self.nslots):
+                self.step(i, self.stream)
         torch.cuda.synchronize(self.device)
+
+    def replay_steps(self, steps: int):
+        """Enqueue exactly `steps` layer steps, rotating the slots."""
+        full, rest = divmod(steps, self.nslots)
+        for _ in range(full):
+            self.round.replay()
+        for i in range(rest):
+            self.graphs[i].replay()
 
     def run(self, warmup: int, steps: int):
         torch = self.torch
-        for i in range(warmup):
-            self.graphs[i % self.nslots].replay()
+        with torch.cuda.stream(self.stream):
+            self.replay_steps(warmup)
         torch.cuda.synchronize(self.device)
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(self.stream):
             start.record(self.stream)
-            for i in range(steps):
-                self.graphs[i % self.nslots].replay()
+            self.replay_steps(steps)
             end.record(self.stream)
         end.synchronize()
         return start.elapsed_time(end) / steps  # ms per step
@@ -201,8 +215,9 @@ class GpuBench:
                     ws=ws)
 
     def time_gateup(self, warmup: int, steps: int):
-        """Average duration of the gate+up kernel (the largest byte mover) per launch,
-        CUDA events on its own stream, rotating weight copies and batches."""
+        """Average duration of a standalone gate+up launch (moe_gateup_swiglu_w4a16 on
+        precomputed descriptors, no prefetch from a router), CUDA events on its own
+        stream, rotating weight copies and batches, replayed from a graph."""
         moe, torch = self.moe, self.torch
         descs = [self.descriptors(i) for i in range(self.nslots)]
         Fmax = max(self.cfg.F, self.cfg.Fs)
@@ -216,18 +231,28 @@ class GpuBench:
                                         stream=self.stream)
 
         with torch.cuda.stream(self.stream):
-            for i in range(warmup):
+            for i in range(self.nslots):
                 launch(i)
+        self.stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(self.nslots):
+                launch(i)
+        reps_w = max(1, warmup // self.nslots)
+        reps = max(1, steps // self.nslots)
+        with torch.cuda.stream(self.stream):
+            for _ in range(reps_w):
+                g.replay()
             self.stream.synchronize()
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
             start.record(self.stream)
-            for i in range(steps):
-                launch(i)
+            for _ in range(reps):
+                g.replay()
             end.record(self.stream)
         end.synchronize()
         active = [int((d["counts"] > 0).sum().item()) for d in descs]
-        return start.elapsed_time(end) / steps, active
+        return start.elapsed_time(end) / (reps * self.nslots), active
 
     def e2e(self, warmup: int, steps: int):
         """moe_layer_forward_host: pinned host x in, pinned host out, captured as a graph."""
@@ -237,27 +262,40 @@ class GpuBench:
         for a, b in zip(xh, self.xs):
             a.copy_(b.cpu())
         oh = torch.empty((T, d), dtype=torch.int16, pin_memory=True)
+        def fwd(i):
+            c = self.copies[i % len(self.copies)]
+            moe.moe_layer_forward_host(xh[i % len(xh)], self.layer.W_r, self.layer.bias,
+                                       self.dims, *c, oh, self.ws, stream=self.stream)
+
         graphs = []
         for i in range(self.nslots):
-            c = self.copies[i % len(self.copies)]
             with torch.cuda.stream(self.stream):
-                moe.moe_layer_forward_host(xh[i % len(xh)], self.layer.W_r, self.layer.bias,
-                                           self.dims, *c, oh, self.ws, stream=self.stream)
+                fwd(i)
             self.stream.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=self.stream):
-                moe.moe_layer_forward_host(xh[i % len(xh)], self.layer.W_r, self.layer.bias,
-                                           self.dims, *c, oh, self.ws, stream=self.stream)
+                fwd(i)
             graphs.append(g)
-        for i in range(warmup):
-            graphs[i % len(graphs)].replay()
+        whole = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(whole, stream=self.stream):
+            for i in range(self.nslots):
+                fwd(i)
+
+        def replay(n):
+            full, rest = divmod(n, self.nslots)
+            for _ in range(full):
+                whole.replay()
+            for i in range(rest):
+                graphs[i].replay()
+
+        with torch.cuda.stream(self.stream):
+            replay(warmup)
         torch.cuda.synchronize(self.device)
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(self.stream):
             start.record(self.stream)
-            for i in range(steps):
-                graphs[i % len(graphs)].replay()
+            replay(steps)
             end.record(self.stream)
         end.synchronize()
         ms = start.elapsed_time(end) / steps
@@ -265,23 +303,29 @@ class GpuBench:
 
     def free(self):
         self.graphs = []
+        self.round = None
         self._keep = []
         self.copies = []
         self.layer = None
         self.torch.cuda.empty_cache()
 
 
-def gpu_roofline_decode(cfg, gu_ms, active, pk, pk_kind):
-    """Gate+up kernel at decode: algorithmic bytes = packed gate+up bytes (+ scales) of the
-    active routed experts and the shared expert, per launch."""
-    per_expert = 2 * cfg.F * cfg.d // 2 + 2 * cfg.F * (cfg.d // cfg.group) * 2
-    shared = 2 * cfg.Fs * cfg.d // 2 + 2 * cfg.Fs * (cfg.d // cfg.group) * 2
-    nbytes = float(np.mean([a * per_expert + shared for a in active]))
-    achieved = nbytes / (gu_ms * 1e-3) / 1e9
+def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms):
+    """The decode step against HBM.  Algorithmic bytes = packed int4 weights + fp16 scales
+    of the active routed experts and of the shared expert (gate+up and down), per step.
+    The step is three launches (fused router, gate+up GEMV, down GEMV + combine) and the
+    router's L2 prefetch moves expert bytes across their boundaries, so the unit is the
+    step (one graph node sequence), timed with CUDA events on its stream."""
+    nbytes = float(np.mean([(a + 1) * cfg.packed_expert_bytes() for a in active]))
+    achieved = nbytes / (ms * 1e-3) / 1e9
     peak = pk["hbm_gbs"]
-    return {"kernel": "gateup_gemv_kernel", "bound": "hbm", "achieved": round(achieved, 1),
-            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": None, "bytes_per_launch": int(nbytes), "launch_us": round(gu_ms * 1e3, 3),
+    router_bytes = cfg.E * cfg.d * 4
+    return {"kernel": "decode step: router_decode_kernel + gateup_gemv_kernel + down_gemv_kernel",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None, "bytes_per_step": int(nbytes),
+            "router_weight_bytes_not_counted": router_bytes,
+            "step_us": round(ms * 1e3, 3),
+            "standalone_gateup_us": round(gu_ms * 1e3, 3),
             "peak_source": f"{pk_kind} hbm_gbs"}
 
 
@@ -392,11 +436,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=HEADLINE, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--secondary", default=SECONDARY, help="extra config in the same line ('' = none)")
+    ap.add_argument("--secondary-steps", type=int, default=400)
     ap.add_argument("--ncopy", type=int, default=8)
     ap.add_argument("--nbatch", type=int, default=8)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -423,7 +468,7 @@ def main():
                               args.nbatch, pk, pk_kind, gpu_index)
     sec_res = None
     if args.secondary and args.secondary != args.config:
-        sec_res = measure_config(args.secondary, device, args.warmup, max(3, args.steps // 10),
+        sec_res = measure_config(args.secondary, device, args.warmup, args.secondary_steps,
                                  args.ncopy, args.nbatch, pk, pk_kind, gpu_index)
     ms = main_res["ms"]
     if world > 1:
@@ -441,8 +486,7 @@ def main():
                          f"{sec:.1f} s of single-thread CPU work"}
 
     if rank == 0:
-        roof = gpu_roofline_decode(cfg, main_res["gu_ms"], main_res["active"], pk, pk_kind)
-        layer_gbs = main_res["layer_bytes"] / (ms * 1e-3) / 1e9
+        roof = gpu_roofline_decode(cfg, ms, main_res["active"], pk, pk_kind, main_res["gu_ms"])
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -458,9 +502,6 @@ def main():
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
             "roofline": roof,
-            "layer_roofline": {"bound": "hbm", "bytes_per_step": int(main_res["layer_bytes"]),
-                               "achieved": round(layer_gbs, 1), "peak": pk["hbm_gbs"],
-                               "unit": "GB/s", "frac": round(layer_gbs / pk["hbm_gbs"], 4)},
             "active_experts_mean": float(np.mean(main_res["active"])),
             "clocks": main_res["clocks"],
             "e2e": {"value": round(cfg.T / (main_res["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
@@ -468,6 +509,7 @@ def main():
                     "ms_per_step": round(main_res["e2e_ms"], 5),
                     "mode": "graph replay of moe_layer_forward_host (pinned host x and out)"},
             "gpu_launches": kernels_per_step(cfg) * args.steps,
+            "kernels_per_step": kernels_per_step(cfg),
             "cpu_baseline": cpu,
             "peaks": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback",
         }

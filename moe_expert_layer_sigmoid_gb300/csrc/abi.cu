@@ -60,6 +60,14 @@ WsLayout ws_layout(const moe_dims_t& d) {
     return L;
 }
 
+int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!counts[dev]) cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev);
+    return counts[dev];
+}
+
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
     // per (kernel, device) once; a small table is enough for the handful of kernels
@@ -118,7 +126,11 @@ moe_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
     return MOE_OK;
 }
 
-bool w4_ok(moe_w4_t w) { return w.q && w.s; }
+// q is read with 16-byte loads, s with 2-byte loads.
+bool w4_ok(moe_w4_t w) {
+    return w.q && w.s && reinterpret_cast<uintptr_t>(w.q) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(w.s) % 2 == 0;
+}
 
 template <typename T>
 T* ws_at(void* ws, size_t off) {
@@ -144,7 +156,8 @@ moe_status_t gateup_impl(const uint16_t* x, const moe_dims_t& d, const int32_t* 
     WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
     switch (expert_path(d)) {
         case Path::kGemv:
-            return map_err(launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, hdr, st));
+            return map_err(launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, nullptr,
+                                              hdr, false, st));
         case Path::kGrouped:
             return map_err(launch_gateup_grouped(x, d, perm, Wgu, Wgu_s, H, hdr,
                                                  ws_at<int4>(ws, L.tiles), ws_at<uint16_t>(ws, L.xs),
@@ -160,7 +173,8 @@ moe_status_t down_impl(const uint16_t* H, const moe_dims_t& d, const int32_t* of
     WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
     switch (expert_path(d)) {
         case Path::kGemv:
-            return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, hdr, st));
+            return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, nullptr, nullptr,
+                                            nullptr, nullptr, hdr, false, st));
         case Path::kGrouped:
             return map_err(launch_down_grouped(H, d, Wd, Wd_s, Y, hdr,
                                                ws_at<int4>(ws, L.tiles) + L.max_tiles, st));
@@ -294,8 +308,34 @@ moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float*
     uint16_t* H = ws_at<uint16_t>(ws, L.H);
     float* Y = ws_at<float>(ws, L.Y);
     WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
-    cudaError_t e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
-                                  ws_at<float>(ws, L.logits), L.router_ksplit, s);
+    const Path path = expert_path(d);
+    if (path == Path::kUnsupported) return MOE_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (path == Path::kGemv) {
+        // decode chain: fused router + descriptors, then the two GEMVs with the
+        // combine fused into the down kernel; each waits on its predecessor
+        // through programmatic dependent launch
+        if (d.T <= kMaxDecodeT) {
+            e = launch_router_decode(x, W_r, bias, d, topk_idx, topk_w, nullptr,
+                                     ws_at<float>(ws, L.logits), L.router_ksplit, counts, offsets,
+                                     perm, pos, sched, hdr, s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+        } else {
+            e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
+                              ws_at<float>(ws, L.logits), L.router_ksplit, s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
+                                   ws_at<int4>(ws, L.tiles), L.max_tiles, s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+        }
+        e = launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, &hdr->n_active, hdr,
+                               true, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, &hdr->n_active, topk_w,
+                                        pos, out, hdr, true, s));
+    }
+    e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr, ws_at<float>(ws, L.logits),
+                      L.router_ksplit, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
                            ws_at<int4>(ws, L.tiles), L.max_tiles, s);

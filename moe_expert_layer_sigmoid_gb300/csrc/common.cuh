@@ -62,6 +62,10 @@ constexpr int kRouterKChunk = 1024;
 // GEMV (decode) expert path for T <= kGemvMaxT unless forced.
 constexpr int kGemvMaxT = 64;
 
+// Fused decode router (decode.cu) limits.
+constexpr int kMaxDecodeT = 64;
+constexpr int kMaxExperts = 1024;
+
 // Grouped-GEMM tile geometry (weight rows x tokens).
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
@@ -82,13 +86,28 @@ cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int
                                int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,
                                WsHeader* hdr, int4* tiles, int64_t max_tiles, cudaStream_t st);
 
+// Decode expert GEMVs (experts_gemv.cu).  `n_active` is the count of routed
+// groups with rows (the workspace header's, written by the fused router) or
+// null, in which case the kernels count them from offsets and sched.  `pdl`
+// launches with programmatic stream serialisation: the kernel's prologue
+// overlaps the previous kernel, and it waits for it before reading its
+// outputs.  With `out` non-null the down kernel also does the combine.
 cudaError_t launch_gateup_gemv(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,
                                const int32_t* perm, const int32_t* sched, moe_w4_t Wgu,
-                               moe_w4_t Wgu_s, uint16_t* H, WsHeader* hdr, cudaStream_t st);
+                               moe_w4_t Wgu_s, uint16_t* H, const int32_t* n_active,
+                               WsHeader* hdr, bool pdl, cudaStream_t st);
 
 cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32_t* offsets,
                              const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y,
-                             WsHeader* hdr, cudaStream_t st);
+                             const int32_t* n_active, const float* topk_w, const int32_t* pos,
+                             uint16_t* out, WsHeader* hdr, bool pdl, cudaStream_t st);
+
+// Fused decode router: logits, top-k and descriptors in one launch (T <= 64).
+cudaError_t launch_router_decode(const uint16_t* x, const float* W_r, const float* bias,
+                                 const moe_dims_t& d, int32_t* topk_idx, float* topk_w,
+                                 float* margin, float* logits, int ksplit, int32_t* counts,
+                                 int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,
+                                 WsHeader* hdr, cudaStream_t st);
 
 // Grouped tcgen05 path (prefill).  `tiles` is the tile schedule that
 // launch_descriptors wrote into the workspace (two lists of max_tiles each).
@@ -104,6 +123,9 @@ cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t
 
 cudaError_t launch_combine(const float* Y, const float* topk_w, const int32_t* pos,
                            const moe_dims_t& d, uint16_t* out, cudaStream_t st);
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
 
 // Raise a kernel's dynamic shared-memory limit when `bytes` exceeds the 48 KB
 // default (once per kernel and device; safe to call during stream capture).
@@ -124,5 +146,14 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 }
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue / wait until the previous kernel has completed and its writes are
+// visible.  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 
 }  // namespace moe

@@ -2,49 +2,158 @@
 //
 // The Laguna decode path runs the MoE gate+up projection fused (SwiGLU) and the
 // shared expert through the same gathered kernel (thewafflehaus/butter PR #69,
-// commit "feat(laguna): Laguna-S-2.1 decode on the CUDA engine").  Here one CTA
-// owns a band of output rows of one expert (or of the shared expert) and
-// every token routed to it; weights stream from HBM once per token tile with
-// coalesced 16-byte loads (32 nibbles per load, one group scale per load),
-// activations are gathered through the descriptor permutation into shared
-// memory.
+// commit "feat(laguna): Laguna-S-2.1 decode on the CUDA engine").  Here both
+// projections are persistent kernels with one CTA per SM:
 //
-// Arithmetic: a 32-element chunk is contracted against exact integer q values
-// (q = nibble, made an fp32 integer by the 2^23 exponent trick) and the
-// chunk's fp32 partial sum is multiplied by its group scale; since q * s is the
-// dequantised weight exactly, this computes sum_i x_i * (q_i * s) with only
-// fp32 summation rounding.
-#include "common.cuh"
+//   gate+up  work item = one gate row and its up row of one group (a routed
+//            expert in schedule order, or the shared expert) against every
+//            token of the group; each CTA takes an equal contiguous share of
+//            the items, the shared expert's before the routed experts'.  The
+//            shared expert depends on x alone, so it runs before the kernel
+//            waits for the router (programmatic dependent launch).
+//   down     each CTA owns a contiguous range of output channels for every
+//            group; work item = four channels of one group.  With the combine
+//            fused in, the CTA then sums its channels' routed rows and shared
+//            row in the fixed order of moe_combine_shared.
+//
+// Staging.  Each warp runs its own ring of shared-memory stages filled by the
+// TMA unit (cp.async.bulk, completion on one mbarrier per stage): while it
+// computes one item, the rows of its next items are already in flight, so
+// each SM keeps about 190 KB of weight reads outstanding.  A lane then reads
+// 16 bytes (32 nibbles, one quantisation-group scale) per shared-memory load.
+// Shapes whose scale rows are not 16-byte multiples use the same arithmetic
+// with 16-byte global loads instead (the load path).
+//
+// Launch order (programmatic dependent launch): the gate+up kernel requests
+// its shared-expert stages and loads x before it waits for the router, and
+// lets the down kernel launch once the routing is complete; the down kernel
+// requests its first weight stages before it waits for H.
+//
+// Arithmetic.  Decode streams about two int4 weights per HBM byte, so the
+// kernel has only a few lane-operations per weight.  One lop3 turns bits 0-3
+// and 16-19 of a word into the bf16 pair {136 + q, 136 + q'} exactly (mantissa
+// field of 128.0 = 0x4300, nibble xor 8 = q + 8), so a 32-bit word of eight
+// nibbles costs three shifts and four lop3; the products use the mixed
+// fma.rn.f32.bf16 (bf16 x bf16 + fp32), exact products with fp32 accumulation.
+//   T = 1:  the offset is taken out per 32-element chunk, sum x * q =
+//           sum x * (136 + q) - 136 * sum x, with the chunk sums of x kept in
+//           registers beside x itself.
+//   T > 1:  each pair is first made exact q by one fma.rn.bf16x2 (t - 136),
+//           then reused for every token of the pass.
+// Each chunk's fp32 partial is multiplied by its fp16 scale and accumulated,
+// so the result is sum x * (q * s) with fp32 summation rounding only.
+#include "async.cuh"
 
 namespace moe {
 namespace {
 
-// Offset-binary nibble u = q + 8 in the low mantissa bits of 2^23: value 2^23 + u.
-constexpr float kMagicOffset = 8388616.0f;  // 2^23 + 8
+constexpr int kGemvWarps = 16;
+constexpr int kGemvThreads = kGemvWarps * 32;
+constexpr int kGuTokPass = 4;  // tokens per pass of the gate+up kernel (T > 1)
+constexpr int kDnTokPass = 2;  // tokens per pass of the down kernel (T > 1)
+constexpr int kDnQuad = 4;     // output channels per down work item
 
-__device__ __forceinline__ float dot8_q4(uint32_t w, uint4 xv) {
-    const uint32_t u = w ^ 0x88888888u;  // two's complement nibble -> offset binary
-    float q[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) q[j] = __uint_as_float(0x4B000000u | ((u >> (4 * j)) & 0xFu)) - kMagicOffset;
-    float a = q[0] * bf16_lo(xv.x);
-    a = fmaf(q[1], bf16_hi(xv.x), a);
-    a = fmaf(q[2], bf16_lo(xv.y), a);
-    a = fmaf(q[3], bf16_hi(xv.y), a);
-    a = fmaf(q[4], bf16_lo(xv.z), a);
-    a = fmaf(q[5], bf16_hi(xv.z), a);
-    a = fmaf(q[6], bf16_lo(xv.w), a);
-    a = fmaf(q[7], bf16_hi(xv.w), a);
-    return a;
+// 16-byte load of streamed weights: read once, so no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
 }
 
-// 32 nibbles (one 16-byte load) against 32 bf16 activations (four 16-byte words).
-__device__ __forceinline__ float dot32_q4(uint4 w, const uint4* xs) {
-    float a = dot8_q4(w.x, xs[0]);
-    a += dot8_q4(w.y, xs[1]);
-    a += dot8_q4(w.z, xs[2]);
-    a += dot8_q4(w.w, xs[3]);
-    return a;
+// bits 0-3 and 16-19 of v -> bf16 pair {136 + q_lo, 136 + q_hi}
+__device__ __forceinline__ uint32_t nib_pair(uint32_t v) {
+    uint32_t t;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(t) : "r"(v), "r"(0x000F000Fu), "r"(0x43084308u));
+    return t;
+}
+
+// exact q pair: t * 1 - 136 in bf16x2 (both values are small integers)
+__device__ __forceinline__ uint32_t q_pair(uint32_t v) {
+    uint32_t q;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(nib_pair(v)), "r"(0x3F803F80u), "r"(0xC308C308u));
+    return q;
+}
+
+// acc += lo(p) * half_S(xa) + hi(p) * half_S(xb), S = 0 low halves, 1 high.
+template <int S>
+__device__ __forceinline__ float fma_pair(float acc, uint32_t p, uint32_t xa, uint32_t xb) {
+    if (S == 0)
+        asm("{\n .reg .b16 pl, ph, al, ah, bl, bh;\n mov.b32 {pl, ph}, %1;\n mov.b32 {al, ah}, %2;\n"
+            " mov.b32 {bl, bh}, %3;\n fma.rn.f32.bf16 %0, pl, al, %0;\n fma.rn.f32.bf16 %0, ph, bl, %0;\n}"
+            : "+f"(acc)
+            : "r"(p), "r"(xa), "r"(xb));
+    else
+        asm("{\n .reg .b16 pl, ph, al, ah, bl, bh;\n mov.b32 {pl, ph}, %1;\n mov.b32 {al, ah}, %2;\n"
+            " mov.b32 {bl, bh}, %3;\n fma.rn.f32.bf16 %0, pl, ah, %0;\n fma.rn.f32.bf16 %0, ph, bh, %0;\n}"
+            : "+f"(acc)
+            : "r"(p), "r"(xa), "r"(xb));
+    return acc;
+}
+
+// Eight nibbles of w (element 2j in the low nibble of byte j) against the
+// eight bf16 activations xv.  Element pairs are (j, j + 4): word w >> 4j gives
+// element j in bits 0-3 and element j + 4 in bits 16-19.  Four accumulators
+// (one per j) keep four independent FMA chains.
+// Offset form: acc[j] += x * (136 + q).
+__device__ __forceinline__ void dot8_off(uint32_t w, uint4 xv, float* acc) {
+    acc[0] = fma_pair<0>(acc[0], nib_pair(w), xv.x, xv.z);
+    acc[1] = fma_pair<1>(acc[1], nib_pair(w >> 4), xv.x, xv.z);
+    acc[2] = fma_pair<0>(acc[2], nib_pair(w >> 8), xv.y, xv.w);
+    acc[3] = fma_pair<1>(acc[3], nib_pair(w >> 12), xv.y, xv.w);
+}
+
+// Exact form on pre-made q pairs qp[0..3] of one word.
+__device__ __forceinline__ void dot8_q(const uint32_t* qp, uint4 xv, float* acc) {
+    acc[0] = fma_pair<0>(acc[0], qp[0], xv.x, xv.z);
+    acc[1] = fma_pair<1>(acc[1], qp[1], xv.x, xv.z);
+    acc[2] = fma_pair<0>(acc[2], qp[2], xv.y, xv.w);
+    acc[3] = fma_pair<1>(acc[3], qp[3], xv.y, xv.w);
+}
+
+__device__ __forceinline__ void q_pairs32(uint4 w, uint32_t* qp) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        qp[4 * i + 0] = q_pair(ws[i]);
+        qp[4 * i + 1] = q_pair(ws[i] >> 4);
+        qp[4 * i + 2] = q_pair(ws[i] >> 8);
+        qp[4 * i + 3] = q_pair(ws[i] >> 12);
+    }
+}
+
+__device__ __forceinline__ float sum4(const float* a) { return (a[0] + a[1]) + (a[2] + a[3]); }
+
+// sum over a 32-element chunk of x * (136 + q)
+__device__ __forceinline__ float dot32_off(uint4 w, const uint4* xv) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    dot8_off(w.x, xv[0], acc);
+    dot8_off(w.y, xv[1], acc);
+    dot8_off(w.z, xv[2], acc);
+    dot8_off(w.w, xv[3], acc);
+    return sum4(acc);
+}
+
+// sum over a 32-element chunk of x * q
+__device__ __forceinline__ float dot32_q(const uint32_t* qp, const uint4* xv) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    dot8_q(qp, xv[0], acc);
+    dot8_q(qp + 4, xv[1], acc);
+    dot8_q(qp + 8, xv[2], acc);
+    dot8_q(qp + 12, xv[3], acc);
+    return sum4(acc);
+}
+
+__device__ __forceinline__ float sum32_bf16(const uint4* xv) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t p[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s += bf16_lo(p[j]) + bf16_hi(p[j]);
+    }
+    return s;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -53,188 +162,762 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Group descriptor of blockIdx.y: a routed expert in schedule order, or the
-// shared expert after the last routed group.
-struct GroupRef {
-    int64_t row0;  // first row of H / Y
-    int count;     // rows (tokens) in the group
-    int Fg;        // FFN width of the group
-    int expert;    // -1 for the shared expert
-};
-
-__device__ __forceinline__ GroupRef group_of(int y, int n_route_groups, int T, int k, int F,
-                                             int Fs, const int32_t* offsets, const int32_t* sched) {
-    GroupRef g;
-    if (y < n_route_groups) {
-        const int e = sched[y];
-        g.expert = e;
-        g.row0 = offsets[e];
-        g.count = offsets[e + 1] - offsets[e];
-        g.Fg = F;
-    } else {
-        g.expert = -1;
-        g.row0 = (int64_t)T * k;
-        g.count = T;
-        g.Fg = Fs;
-    }
-    return g;
+__device__ __forceinline__ void load_chunk(const uint16_t* row, int c, uint4* xv) {
+    const uint4* p = reinterpret_cast<const uint4*>(row) + 4 * c;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) xv[v] = __ldg(p + v);
 }
 
-constexpr int kGuRowPairsPerWarp = 2;
-constexpr int kGuRowsPerCta = 8 * kGuRowPairsPerWarp;  // gate rows (and as many up rows) per CTA
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
-template <int TOK>
-__global__ void __launch_bounds__(256)
-gateup_gemv_kernel(const uint16_t* __restrict__ x, int T, int d, int k, int F, int Fs, int group,
-                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
-                   const int32_t* __restrict__ sched, const uint8_t* __restrict__ q_r,
-                   const __half* __restrict__ s_r, const uint8_t* __restrict__ q_sh,
-                   const __half* __restrict__ s_sh, uint16_t* __restrict__ H, int ldh,
-                   int n_route_groups) {
-    extern __shared__ uint4 xs[];  // [TOK][d / 8]
-    const GroupRef g = group_of(blockIdx.y, n_route_groups, T, k, F, Fs, offsets, sched);
-    if (g.count == 0) return;
-    const int f0 = blockIdx.x * kGuRowsPerCta;
-    if (f0 >= g.Fg) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d8 = d / 8, nchunk = d / 32, ngr = d / group;
-    const uint8_t* qg = g.expert >= 0 ? q_r + (int64_t)g.expert * 2 * F * (d / 2) : q_sh;
-    const __half* sg = g.expert >= 0 ? s_r + (int64_t)g.expert * 2 * F * ngr : s_sh;
-
-    for (int i0 = 0; i0 < g.count; i0 += TOK) {
-        const int ntok = min(TOK, g.count - i0);
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < ntok * d8; idx += blockDim.x) {
-            const int tt = idx / d8, c8 = idx - tt * d8;
-            const int64_t row = g.row0 + i0 + tt;
-            const int tok = g.expert >= 0 ? perm[row] / k : (int)(row - g.row0);
-            xs[tt * d8 + c8] = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)tok * d) + c8);
+// Number of routed groups with rows: from the header, or counted (sched is
+// ordered by count, so the active experts are a prefix).  Block-uniform.
+__device__ __forceinline__ int active_groups(const int32_t* n_active, const int32_t* offsets,
+                                             const int32_t* sched, int n_route_max) {
+    if (n_active) return *n_active;
+    int n = 0;
+    for (int y0 = 0; y0 < n_route_max; y0 += blockDim.x) {
+        const int y = y0 + threadIdx.x;
+        bool act = false;
+        if (y < n_route_max) {
+            const int e = sched[y];
+            act = offsets[e + 1] > offsets[e];
         }
-        __syncthreads();
+        n += __syncthreads_count(act);
+    }
+    return n;
+}
+
+// ---------------------------------------------------------------------------
+constexpr int kMaxRing = 6;                     // stages per warp, at most
+constexpr int kRingSmemBudget = 200 * 1024;     // dynamic shared memory of a ring kernel
+constexpr size_t kMaxStagedH = 64 * 1024;       // H rows staged by the down kernel, at most
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float lds_f16(uint32_t addr) {
+    unsigned short h;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
+    return __half2float(__ushort_as_half(h));
+}
+
+// A row (16-byte words) and its scale row, in global memory (load path) or in
+// a ring stage (shared-memory addresses).
+struct RowRef {
+    const uint4* q;
+    const __half* s;
+    uint32_t sq, ss;
+};
+
+template <bool SMEM>
+__device__ __forceinline__ uint4 row_word(const RowRef& r, int c) {
+    if constexpr (SMEM)
+        return lds128(r.sq + 16u * (uint32_t)c);
+    else
+        return ld_stream(r.q + c);
+}
+template <bool SMEM>
+__device__ __forceinline__ float row_scale(const RowRef& r, int i) {
+    if constexpr (SMEM)
+        return lds_f16(r.ss + 2u * (uint32_t)i);
+    else
+        return __half2float(r.s[i]);
+}
+
+// Rows [row0, row0 + count) of H / Y belong to a group: a routed expert's rows
+// (offsets) or the shared expert's (after the T*k routed rows).
+__device__ __forceinline__ void group_rows(const int32_t* offsets, int T, int k, int expert,
+                                           int* row0, int* count) {
+    if (expert >= 0) {
+        *row0 = offsets[expert];
+        *count = offsets[expert + 1] - *row0;
+    } else {
+        *row0 = T * k;
+        *count = T;
+    }
+}
+
+struct GuArgs {
+    const uint16_t* x;
+    int T, d, k, F, Fs, gsh;  // chunk c (32 elements) uses scale index c >> gsh
+    const int32_t* offsets;
+    const int32_t* perm;
+    const int32_t* sched;
+    const uint8_t* q_r;
+    const __half* s_r;
+    const uint8_t* q_sh;
+    const __half* s_sh;
+    uint16_t* H;
+    int ldh;
+    int n_route_max;
+    const int32_t* n_active;
+    WsHeader* hdr;
+};
+
+// Where the gate and up rows of one item are, with their scale rows.
+struct GuRows {
+    RowRef g, u;
+};
+
+__device__ __forceinline__ GuRows gu_rows_global(const GuArgs& a, int expert, int f) {
+    const int ngr = (a.d >> 5) >> a.gsh;
+    const int Fg = expert >= 0 ? a.F : a.Fs;
+    const int64_t rowb = a.d / 2;
+    const uint8_t* qb = expert >= 0 ? a.q_r + (int64_t)expert * 2 * a.F * rowb : a.q_sh;
+    const __half* sb = expert >= 0 ? a.s_r + (int64_t)expert * 2 * a.F * ngr : a.s_sh;
+    GuRows r;
+    r.g.q = reinterpret_cast<const uint4*>(qb + (int64_t)f * rowb);
+    r.u.q = reinterpret_cast<const uint4*>(qb + (int64_t)(Fg + f) * rowb);
+    r.g.s = sb + (int64_t)f * ngr;
+    r.u.s = sb + (int64_t)(Fg + f) * ngr;
+    r.g.sq = r.g.ss = r.u.sq = r.u.ss = 0;
+    return r;
+}
+
+// One gate+up item: row pair f of `expert` (-1: the shared expert) against the
+// group's rows [row0, row0 + count), writing SwiGLU(gate, up) to H.
+// ONE: T == 1 and the lane's x chunks (and their sums) are in xr / xs.
+template <int CPL, bool ONE, bool SMEM>
+__device__ __forceinline__ void gu_compute(const GuArgs& a, int expert, int f, const GuRows& w,
+                                           int row0, int count, const uint4 (&xr)[CPL][4],
+                                           const float (&xs)[CPL], int lane) {
+    const int nc = a.d >> 5;
+    if constexpr (ONE) {
+        float ag = 0.f, au = 0.f;
 #pragma unroll
-        for (int p = 0; p < kGuRowPairsPerWarp; ++p) {
-            const int f = f0 + warp * kGuRowPairsPerWarp + p;
-            const uint4* gq = reinterpret_cast<const uint4*>(qg + (int64_t)f * (d / 2));
-            const uint4* uq = reinterpret_cast<const uint4*>(qg + (int64_t)(g.Fg + f) * (d / 2));
-            const __half* gsc = sg + (int64_t)f * ngr;
-            const __half* usc = sg + (int64_t)(g.Fg + f) * ngr;
-            float accg[TOK], accu[TOK];
+        for (int i = 0; i < CPL; ++i) {
+            const int c = lane + 32 * i;
+            if (c < nc) {
+                const uint4 wg = row_word<SMEM>(w.g, c), wu = row_word<SMEM>(w.u, c);
+                const float sg = row_scale<SMEM>(w.g, c >> a.gsh);
+                const float su = row_scale<SMEM>(w.u, c >> a.gsh);
+                const float pg = fmaf(-136.f, xs[i], dot32_off(wg, xr[i]));
+                const float pu = fmaf(-136.f, xs[i], dot32_off(wu, xr[i]));
+                ag = fmaf(sg, pg, ag);
+                au = fmaf(su, pu, au);
+            }
+        }
+        ag = warp_sum(ag);
+        au = warp_sum(au);
+        if (lane == 0 && count > 0)
+            a.H[(int64_t)row0 * a.ldh + f] = float_to_bf16_bits(swiglu(ag, au));
+    } else {
+        for (int i0 = 0; i0 < count; i0 += kGuTokPass) {
+            const int ntok = min(kGuTokPass, count - i0);
+            const uint16_t* xrow[kGuTokPass];
 #pragma unroll
-            for (int tt = 0; tt < TOK; ++tt) accg[tt] = accu[tt] = 0.f;
-            for (int c = lane; c < nchunk; c += 32) {
-                const uint4 wg = __ldg(gq + c), wu = __ldg(uq + c);
-                const float scg = __half2float(gsc[(32 * c) / group]);
-                const float scu = __half2float(usc[(32 * c) / group]);
+            for (int tt = 0; tt < kGuTokPass; ++tt) {
+                const int r = row0 + i0 + min(tt, ntok - 1);
+                const int tok = expert >= 0 ? a.perm[r] / a.k : r - row0;
+                xrow[tt] = a.x + (int64_t)tok * a.d;
+            }
+            float ag[kGuTokPass], au[kGuTokPass];
 #pragma unroll
-                for (int tt = 0; tt < TOK; ++tt) {
-                    if (tt < ntok) {
-                        const uint4* xv = xs + tt * d8 + 4 * c;
-                        accg[tt] = fmaf(scg, dot32_q4(wg, xv), accg[tt]);
-                        accu[tt] = fmaf(scu, dot32_q4(wu, xv), accu[tt]);
+            for (int tt = 0; tt < kGuTokPass; ++tt) ag[tt] = au[tt] = 0.f;
+            for (int cb = 0; cb < nc; cb += 32 * CPL) {
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    const int c = cb + lane + 32 * i;
+                    if (c >= nc) continue;
+                    uint32_t qg[16], qu[16];
+                    q_pairs32(row_word<SMEM>(w.g, c), qg);
+                    q_pairs32(row_word<SMEM>(w.u, c), qu);
+                    const float sg = row_scale<SMEM>(w.g, c >> a.gsh);
+                    const float su = row_scale<SMEM>(w.u, c >> a.gsh);
+#pragma unroll
+                    for (int tt = 0; tt < kGuTokPass; ++tt) {
+                        if (tt < ntok) {
+                            uint4 xv[4];
+                            load_chunk(xrow[tt], c, xv);
+                            ag[tt] = fmaf(sg, dot32_q(qg, xv), ag[tt]);
+                            au[tt] = fmaf(su, dot32_q(qu, xv), au[tt]);
+                        }
                     }
                 }
             }
 #pragma unroll
-            for (int tt = 0; tt < TOK; ++tt) {
-                const float gv = warp_sum(accg[tt]);
-                const float uv = warp_sum(accu[tt]);
-                if (lane == 0 && tt < ntok) {
-                    const float h = gv / (1.0f + expf(-gv)) * uv;
-                    H[(g.row0 + i0 + tt) * ldh + f] = float_to_bf16_bits(h);
+            for (int tt = 0; tt < kGuTokPass; ++tt) {
+                if (tt < ntok) {
+                    const float g = warp_sum(ag[tt]);
+                    const float u = warp_sum(au[tt]);
+                    if (lane == 0)
+                        a.H[(int64_t)(row0 + i0 + tt) * a.ldh + f] = float_to_bf16_bits(swiglu(g, u));
                 }
             }
         }
     }
 }
 
-constexpr int kDnRowsPerWarp = 4;
-constexpr int kDnRowsPerCta = 8 * kDnRowsPerWarp;
-
-template <int TOK>
-__global__ void __launch_bounds__(256)
-down_gemv_kernel(const uint16_t* __restrict__ H, int ldh, int T, int d, int k, int F, int Fs,
-                 int group, const int32_t* __restrict__ offsets, const int32_t* __restrict__ sched,
-                 const uint8_t* __restrict__ q_r, const __half* __restrict__ s_r,
-                 const uint8_t* __restrict__ q_sh, const __half* __restrict__ s_sh,
-                 float* __restrict__ Y, int n_route_groups) {
-    extern __shared__ uint4 hs[];  // [TOK][Fg / 8]
-    const GroupRef g = group_of(blockIdx.y, n_route_groups, T, k, F, Fs, offsets, sched);
-    if (g.count == 0) return;
-    const int c0 = blockIdx.x * kDnRowsPerCta;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int K = g.Fg, k8 = K / 8, nchunk = K / 32, ngr = K / group;
-    const uint8_t* qd = g.expert >= 0 ? q_r + (int64_t)g.expert * d * (F / 2) : q_sh;
-    const __half* sd = g.expert >= 0 ? s_r + (int64_t)g.expert * d * (F / group) : s_sh;
-
-    for (int i0 = 0; i0 < g.count; i0 += TOK) {
-        const int ntok = min(TOK, g.count - i0);
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < ntok * k8; idx += blockDim.x) {
-            const int tt = idx / k8, c8 = idx - tt * k8;
-            hs[tt * k8 + c8] =
-                __ldg(reinterpret_cast<const uint4*>(H + (g.row0 + i0 + tt) * ldh) + c8);
+// x chunks of the lane (chunk c = lane + 32 i) and their sums, for T == 1.
+template <int CPL>
+__device__ __forceinline__ void load_x_regs(const uint16_t* x, int d, int lane, uint4 (&xr)[CPL][4],
+                                            float (&xs)[CPL]) {
+    const int nc = d >> 5;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nc) {
+            load_chunk(x, c, xr[i]);
+            xs[i] = sum32_bf16(xr[i]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) xr[i][v] = make_uint4(0, 0, 0, 0);
+            xs[i] = 0.f;
         }
-        __syncthreads();
+    }
+}
+
+// Item of the routed phase: (expert, row pair).
+__device__ __forceinline__ void gu_routed_item(const GuArgs& a, int64_t it, int* expert, int* f) {
+    const int y = (int)(it / a.F);
+    *f = (int)(it - (int64_t)y * a.F);
+    *expert = a.sched[y];
+}
+
+// Load path.
+template <int CPL, bool ONE>
+__global__ void __launch_bounds__(kGemvThreads, 1) gateup_gemv_kernel(const GuArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, b = blockIdx.x;
+    uint4 xr[CPL][4];
+    float xs[CPL];
+    if (ONE) load_x_regs<CPL>(a.x, a.d, lane, xr, xs);
+    // the shared expert reads only x: it runs before the wait for the router
+    {
+        const int lo = (int)((int64_t)b * a.Fs / G), hi = (int)((int64_t)(b + 1) * a.Fs / G);
+        for (int f = lo + warp; f < hi; f += kGemvWarps) {
+            int row0, count;
+            group_rows(a.offsets, a.T, a.k, -1, &row0, &count);
+            gu_compute<CPL, ONE, false>(a, -1, f, gu_rows_global(a, -1, f), row0, count, xr, xs, lane);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();  // after the wait: dependents may read the routing early
+    const int n_act = active_groups(a.n_active, a.offsets, a.sched, a.n_route_max);
+    const int64_t R = (int64_t)n_act * a.F;
+    const int64_t lo = (int64_t)b * R / G, hi = (int64_t)(b + 1) * R / G;
+    for (int64_t it = lo + warp; it < hi; it += kGemvWarps) {
+        int e, f, row0, count;
+        gu_routed_item(a, it, &e, &f);
+        group_rows(a.offsets, a.T, a.k, e, &row0, &count);
+        gu_compute<CPL, ONE, false>(a, e, f, gu_rows_global(a, e, f), row0, count, xr, xs, lane);
+    }
+}
+
+// Ring path.  Stage of one item: [gate q | up q | gate scales | up scales].
+template <int CPL, bool ONE>
+__global__ void __launch_bounds__(kGemvThreads, 1) gateup_ring_kernel(const GuArgs a, int S) {
+    extern __shared__ __align__(128) uint8_t ring_smem[];
+    __shared__ __align__(8) uint64_t s_bar[kGemvWarps * kMaxRing];
+    __shared__ int s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int64_t rowb = a.d / 2;
+    const int scb = ((a.d >> 5) >> a.gsh) * 2;
+    const uint32_t stage_bytes = (uint32_t)(2 * rowb + 2 * scb);
+    uint8_t* wbuf = ring_smem + (size_t)warp * S * stage_bytes;
+    const uint32_t bar0 = smem_u32(&s_bar[warp * kMaxRing]);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kGemvWarps * kMaxRing; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    // Units of this warp, in order: its shared-expert items, then its routed
+    // items.  The shared expert depends on x alone, so its first stages are
+    // requested before the wait for the router; nothing routed is touched
+    // before that wait.
+    const int64_t s_first = (int64_t)b * a.Fs / G + warp, s_hi = (int64_t)(b + 1) * a.Fs / G;
+    const int n_sh = s_first < s_hi ? (int)((s_hi - s_first + kGemvWarps - 1) / kGemvWarps) : 0;
+    int64_t r_first = 0;
+    int n_units = n_sh;
+    auto item = [&](int u, int* e, int* f) {
+        if (u < n_sh) {
+            *e = -1;
+            *f = (int)(s_first + (int64_t)u * kGemvWarps);
+        } else {
+            gu_routed_item(a, r_first + (int64_t)(u - n_sh) * kGemvWarps, e, f);
+        }
+    };
+    auto issue = [&](int u) {  // lane 0
+        int e, f;
+        item(u, &e, &f);
+        const GuRows g = gu_rows_global(a, e, f);
+        const uint32_t slot = u % S;
+        const uint32_t dst = smem_u32(wbuf + slot * stage_bytes);
+        const uint32_t bar = bar0 + 8 * slot;
+        mbar_expect_tx(bar, stage_bytes);
+        bulk_load(dst, g.g.q, (uint32_t)rowb, bar);
+        bulk_load(dst + (uint32_t)rowb, g.u.q, (uint32_t)rowb, bar);
+        bulk_load(dst + 2 * (uint32_t)rowb, g.g.s, scb, bar);
+        bulk_load(dst + 2 * (uint32_t)rowb + scb, g.u.s, scb, bar);
+    };
+    if (lane == 0)
+        for (int u = 0; u < n_sh && u < S; ++u) issue(u);
+
+    uint4 xr[CPL][4];
+    float xs[CPL];
+    if (ONE) load_x_regs<CPL>(a.x, a.d, lane, xr, xs);
+
+    pdl_wait();
+    // dependents launch only once the routing is complete, so they may read it
+    // before their own wait
+    pdl_trigger();
+    const int n_act = active_groups(a.n_active, a.offsets, a.sched, a.n_route_max);
+    {
+        const int64_t R = (int64_t)n_act * a.F;
+        const int64_t lo = (int64_t)b * R / G, hi = (int64_t)(b + 1) * R / G;
+        r_first = lo + warp;
+        n_units += r_first < hi ? (int)((hi - r_first + kGemvWarps - 1) / kGemvWarps) : 0;
+    }
+    if (lane == 0)
+        for (int u = n_sh; u < n_units && u < S; ++u) issue(u);
+    for (int u = 0; u < n_units; ++u) {
+        const uint32_t slot = u % S;
+        if (!mbar_wait(bar0 + 8 * slot, (u / S) & 1, &s_abort, a.hdr)) return;
+        int e, f, row0, count;
+        item(u, &e, &f);
+        group_rows(a.offsets, a.T, a.k, e, &row0, &count);
+        const uint32_t st = smem_u32(wbuf + slot * stage_bytes);
+        GuRows w;
+        w.g.q = w.u.q = nullptr;
+        w.g.s = w.u.s = nullptr;
+        w.g.sq = st;
+        w.u.sq = st + (uint32_t)rowb;
+        w.g.ss = st + 2 * (uint32_t)rowb;
+        w.u.ss = st + 2 * (uint32_t)rowb + scb;
+        gu_compute<CPL, ONE, true>(a, e, f, w, row0, count, xr, xs, lane);
+        __syncwarp();
+        if (lane == 0 && u + S < n_units) {
+            fence_proxy_async_smem();  // the stage was read with plain loads
+            issue(u + S);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Down projection.
+struct DnArgs {
+    const uint16_t* H;
+    int ldh;
+    int T, d, k, F, Fs, gsh;
+    const int32_t* offsets;
+    const int32_t* sched;
+    const uint8_t* q_r;
+    const __half* s_r;
+    const uint8_t* q_sh;
+    const __half* s_sh;
+    float* Y;
+    int n_route_max;
+    const int32_t* n_active;
+    const float* topk_w;  // fused combine when out is non-null
+    const int32_t* pos;
+    uint16_t* out;
+    WsHeader* hdr;
+};
+
+// The kDnQuad consecutive down rows c0 .. c0 + 3 of one group and their scale
+// rows: row ch at q + ch * rowb bytes, its scales at s + ch * ngr (global), or
+// at sq + ch * rowb and ss + 2 * ch * ngr (a ring stage).
+struct DnRows {
+    const uint8_t* q;
+    const __half* s;
+    uint32_t sq, ss;
+};
+
+__device__ __forceinline__ DnRows dn_rows_global(const DnArgs& a, int expert, int c0) {
+    const int K = expert >= 0 ? a.F : a.Fs;
+    const int ngr = (K >> 5) >> a.gsh;
+    const int64_t rowb = K / 2;
+    DnRows r;
+    r.q = (expert >= 0 ? a.q_r + (int64_t)expert * a.d * rowb : a.q_sh) + (int64_t)c0 * rowb;
+    r.s = (expert >= 0 ? a.s_r + (int64_t)expert * a.d * ngr : a.s_sh) + (int64_t)c0 * ngr;
+    r.sq = r.ss = 0;
+    return r;
+}
+
+__device__ __forceinline__ RowRef dn_channel(const DnRows& w, int ch, int64_t rowb, int ngr) {
+    RowRef r;
+    r.q = reinterpret_cast<const uint4*>(w.q + ch * rowb);
+    r.s = w.s + ch * ngr;
+    r.sq = w.sq + (uint32_t)(ch * rowb);
+    r.ss = w.ss + (uint32_t)(2 * ch * ngr);
+    return r;
+}
+
+// One down item: channels c0 .. c0 + 3 of `expert` (-1: shared) for the
+// group's rows [row0, row0 + count), writing Y.
+// hs (ONE only): shared-memory address of the staged H rows (0: read H from
+// global memory).
+template <int CPL, bool ONE, bool SMEM>
+__device__ __forceinline__ void dn_compute(const DnArgs& a, int expert, int c0, const DnRows& w,
+                                           int row0, int count, int lane, uint32_t hs = 0) {
+    const int K = expert >= 0 ? a.F : a.Fs;
+    const int nc = K >> 5, ngr = nc >> a.gsh;
+    const int64_t rowb = K / 2;
+    constexpr int TP = ONE ? 1 : kDnTokPass;
+    for (int i0 = 0; i0 < count; i0 += TP) {
+        const int ntok = min(TP, count - i0);
+        float acc[TP][kDnQuad];
 #pragma unroll
-        for (int r = 0; r < kDnRowsPerWarp; ++r) {
-            const int c = c0 + warp * kDnRowsPerWarp + r;
-            const uint4* wq = reinterpret_cast<const uint4*>(qd + (int64_t)c * (K / 2));
-            const __half* wsc = sd + (int64_t)c * ngr;
-            float acc[TOK];
+        for (int tt = 0; tt < TP; ++tt)
 #pragma unroll
-            for (int tt = 0; tt < TOK; ++tt) acc[tt] = 0.f;
-            for (int ch = lane; ch < nchunk; ch += 32) {
-                const uint4 w = __ldg(wq + ch);
-                const float sc = __half2float(wsc[(32 * ch) / group]);
+            for (int ch = 0; ch < kDnQuad; ++ch) acc[tt][ch] = 0.f;
+        for (int cb = 0; cb < nc; cb += 32 * CPL) {
 #pragma unroll
-                for (int tt = 0; tt < TOK; ++tt)
-                    if (tt < ntok) acc[tt] = fmaf(sc, dot32_q4(w, hs + tt * k8 + 4 * ch), acc[tt]);
+            for (int i = 0; i < CPL; ++i) {
+                const int c = cb + lane + 32 * i;
+                if (c >= nc) continue;
+                if constexpr (ONE) {
+                    uint4 hv[4];
+                    if (hs) {
+                        const uint32_t h = hs + (uint32_t)(row0 * a.ldh + 32 * c) * 2u;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) hv[v] = lds128(h + 16u * v);
+                    } else {
+                        load_chunk(a.H + (int64_t)row0 * a.ldh, c, hv);
+                    }
+                    const float hs = sum32_bf16(hv);
+#pragma unroll
+                    for (int ch = 0; ch < kDnQuad; ++ch) {
+                        const RowRef r = dn_channel(w, ch, rowb, ngr);
+                        const uint4 wq = row_word<SMEM>(r, c);
+                        const float sc = row_scale<SMEM>(r, c >> a.gsh);
+                        const float p = fmaf(-136.f, hs, dot32_off(wq, hv));
+                        acc[0][ch] = fmaf(sc, p, acc[0][ch]);
+                    }
+                } else {
+                    uint4 hv[TP][4];
+#pragma unroll
+                    for (int tt = 0; tt < TP; ++tt)
+                        load_chunk(a.H + (int64_t)(row0 + i0 + min(tt, ntok - 1)) * a.ldh, c, hv[tt]);
+#pragma unroll
+                    for (int ch = 0; ch < kDnQuad; ++ch) {
+                        uint32_t qp[16];
+                        const RowRef r = dn_channel(w, ch, rowb, ngr);
+                        q_pairs32(row_word<SMEM>(r, c), qp);
+                        const float sc = row_scale<SMEM>(r, c >> a.gsh);
+#pragma unroll
+                        for (int tt = 0; tt < TP; ++tt)
+                            acc[tt][ch] = fmaf(sc, dot32_q(qp, hv[tt]), acc[tt][ch]);
+                    }
+                }
             }
+        }
 #pragma unroll
-            for (int tt = 0; tt < TOK; ++tt) {
-                const float v = warp_sum(acc[tt]);
-                if (lane == 0 && tt < ntok) Y[(g.row0 + i0 + tt) * d + c] = v;
+        for (int tt = 0; tt < TP; ++tt) {
+            if (tt < ntok) {
+                float4 v;
+                v.x = warp_sum(acc[tt][0]);
+                v.y = warp_sum(acc[tt][1]);
+                v.z = warp_sum(acc[tt][2]);
+                v.w = warp_sum(acc[tt][3]);
+                if (lane == 0)
+                    *reinterpret_cast<float4*>(a.Y + (int64_t)(row0 + i0 + tt) * a.d + c0) = v;
             }
         }
     }
 }
 
-constexpr int kGemvTok = 4;
+// Output-channel share of CTA b: quads [q_lo, q_hi) of d / 4.
+__device__ __forceinline__ void dn_share(int d, int* q_lo, int* q_hi) {
+    const int nq = d / kDnQuad, G = gridDim.x, b = blockIdx.x;
+    *q_lo = (int)((int64_t)b * nq / G);
+    *q_hi = (int)((int64_t)(b + 1) * nq / G);
+}
+
+// Item it of the CTA's list, group-major: group 0 is the shared expert,
+// group y > 0 the routed expert sched[y - 1].
+__device__ __forceinline__ void dn_item(const DnArgs& a, int it, int nqc, int q_lo, int* expert,
+                                        int* c0) {
+    const int y = it / nqc;
+    *c0 = kDnQuad * (q_lo + (it - y * nqc));
+    *expert = y == 0 ? -1 : a.sched[y - 1];
+}
+
+// Fused combine over this CTA's channels: routed rows in selection order, then
+// the shared row (the order of moe_combine_shared).  Y was written by this
+// CTA, so it is read with plain loads after the barrier.
+__device__ __forceinline__ void dn_combine(const DnArgs& a, int q_lo, int nqc) {
+    __syncthreads();
+    const int T = a.T, k = a.k, d = a.d;
+    for (int idx = threadIdx.x; idx < T * nqc; idx += blockDim.x) {
+        const int t = idx / nqc;
+        const int c = kDnQuad * (q_lo + (idx - t * nqc));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float w = __ldg(a.topk_w + (int64_t)t * k + j);
+            const int64_t r = __ldg(a.pos + (int64_t)t * k + j);
+            const float4 y = *reinterpret_cast<const float4*>(a.Y + r * d + c);
+            acc.x = fmaf(w, y.x, acc.x);
+            acc.y = fmaf(w, y.y, acc.y);
+            acc.z = fmaf(w, y.z, acc.z);
+            acc.w = fmaf(w, y.w, acc.w);
+        }
+        const float4 ys = *reinterpret_cast<const float4*>(a.Y + ((int64_t)T * k + t) * d + c);
+        acc.x += ys.x;
+        acc.y += ys.y;
+        acc.z += ys.z;
+        acc.w += ys.w;
+        uint2 o;
+        o.x = (uint32_t)float_to_bf16_bits(acc.x) | ((uint32_t)float_to_bf16_bits(acc.y) << 16);
+        o.y = (uint32_t)float_to_bf16_bits(acc.z) | ((uint32_t)float_to_bf16_bits(acc.w) << 16);
+        *reinterpret_cast<uint2*>(a.out + (int64_t)t * d + c) = o;
+    }
+}
+
+// Load path.
+template <int CPL, bool ONE>
+__global__ void __launch_bounds__(kGemvThreads, 1) down_gemv_kernel(const DnArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int q_lo, q_hi;
+    dn_share(a.d, &q_lo, &q_hi);
+    const int nqc = q_hi - q_lo;
+    pdl_trigger();
+    pdl_wait();
+    const int n_act = active_groups(a.n_active, a.offsets, a.sched, a.n_route_max);
+    const int items = (1 + n_act) * nqc;
+    for (int it = warp; it < items; it += kGemvWarps) {
+        int e, c0, row0, count;
+        dn_item(a, it, nqc, q_lo, &e, &c0);
+        group_rows(a.offsets, a.T, a.k, e, &row0, &count);
+        dn_compute<CPL, ONE, false>(a, e, c0, dn_rows_global(a, e, c0), row0, count, lane);
+    }
+    if (a.out) dn_combine(a, q_lo, nqc);
+}
+
+// Ring path.  Stage of one item: [4 down rows | their scale rows], the rows
+// of the widest group (max(F, F_s)).  Shared memory: [H rows (h_rows of ldh,
+// T == 1 only) | per-warp rings].
+template <int CPL, bool ONE>
+__global__ void __launch_bounds__(kGemvThreads, 1) down_ring_kernel(const DnArgs a, int S,
+                                                                    int h_rows) {
+    extern __shared__ __align__(128) uint8_t ring_smem[];
+    __shared__ __align__(8) uint64_t s_bar[kGemvWarps * kMaxRing];
+    __shared__ int s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Kmax = max(a.F, a.Fs);
+    const uint32_t q_bytes = (uint32_t)(kDnQuad * (Kmax / 2));
+    const uint32_t stage_bytes = q_bytes + (uint32_t)(kDnQuad * (((Kmax >> 5) >> a.gsh) * 2));
+    const uint32_t h_bytes = (uint32_t)h_rows * a.ldh * 2u;
+    uint8_t* wbuf = ring_smem + h_bytes + (size_t)warp * S * stage_bytes;
+    const uint32_t bar0 = smem_u32(&s_bar[warp * kMaxRing]);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kGemvWarps * kMaxRing; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    int q_lo, q_hi;
+    dn_share(a.d, &q_lo, &q_hi);
+    const int nqc = q_hi - q_lo;
+    pdl_trigger();
+    // The routing is complete here: the gate+up kernel lets this kernel launch
+    // only after its own wait for the router.  So the weight stages are
+    // requested now, and only H (written by the gate+up kernel) waits.
+    const int n_act = active_groups(a.n_active, a.offsets, a.sched, a.n_route_max);
+    const int items = (1 + n_act) * nqc;
+    const int n = warp < items ? (items - warp + kGemvWarps - 1) / kGemvWarps : 0;
+    auto issue = [&](int u) {  // lane 0
+        int e, c0;
+        dn_item(a, warp + u * kGemvWarps, nqc, q_lo, &e, &c0);
+        const DnRows g = dn_rows_global(a, e, c0);
+        const int K = e >= 0 ? a.F : a.Fs;
+        const uint32_t qb = (uint32_t)(kDnQuad * (K / 2));
+        const uint32_t sb = (uint32_t)(kDnQuad * (((K >> 5) >> a.gsh) * 2));
+        const uint32_t slot = u % S;
+        const uint32_t dst = smem_u32(wbuf + slot * stage_bytes);
+        const uint32_t bar = bar0 + 8 * slot;
+        mbar_expect_tx(bar, qb + sb);
+        bulk_load(dst, g.q, qb, bar);
+        bulk_load(dst + q_bytes, g.s, sb, bar);
+    };
+    if (lane == 0)
+        for (int u = 0; u < n && u < S; ++u) issue(u);
+    pdl_wait();
+    uint32_t hs = 0;
+    if (h_rows) {  // H rows of a single token, staged once for every item
+        const uint4* src = reinterpret_cast<const uint4*>(a.H);
+        uint4* dst = reinterpret_cast<uint4*>(ring_smem);
+        for (uint32_t i = threadIdx.x; i < h_bytes / 16; i += kGemvThreads) dst[i] = __ldg(src + i);
+        __syncthreads();
+        hs = smem_u32(ring_smem);
+    }
+    for (int u = 0; u < n; ++u) {
+        const uint32_t slot = u % S;
+        if (!mbar_wait(bar0 + 8 * slot, (u / S) & 1, &s_abort, a.hdr)) break;
+        int e, c0, row0, count;
+        dn_item(a, warp + u * kGemvWarps, nqc, q_lo, &e, &c0);
+        group_rows(a.offsets, a.T, a.k, e, &row0, &count);
+        DnRows w;
+        w.q = nullptr;
+        w.s = nullptr;
+        w.sq = smem_u32(wbuf + slot * stage_bytes);
+        w.ss = w.sq + q_bytes;
+        dn_compute<CPL, ONE, true>(a, e, c0, w, row0, count, lane, hs);
+        __syncwarp();
+        if (lane == 0 && u + S < n) {
+            fence_proxy_async_smem();  // the stage was read with plain loads
+            issue(u + S);
+        }
+    }
+    if (a.out) dn_combine(a, q_lo, nqc);
+}
+
+// ---------------------------------------------------------------------------
+int log2_group_chunks(int group) { return group == 32 ? 0 : group == 64 ? 1 : 2; }
+
+// 16-byte loads per lane and row in one pass over K; longer rows take several
+// passes (register budget of 128 per thread at 512 threads).
+int chunks_per_lane(int K, int cap) {
+    const int nc = K / 32;
+    const int c = (nc + 31) / 32;
+    return std::min(cap, c <= 1 ? 1 : c <= 2 ? 2 : 4);
+}
+
+// Stages per warp that fit the ring budget less `other` bytes (0: the ring
+// path does not apply).
+int ring_stages(size_t stage_bytes, size_t other = 0) {
+    if (other >= (size_t)kRingSmemBudget) return 0;
+    const size_t per_warp = (kRingSmemBudget - other) / kGemvWarps;
+    return (int)std::min<size_t>(kMaxRing, per_warp / stage_bytes);
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_persistent(Kern kern, size_t smem, bool pdl, cudaStream_t st, Args... args) {
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    if (smem) {
+        cudaError_t err = ensure_dynamic_smem((const void*)kern, smem);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int CPL>
+cudaError_t launch_gu(const GuArgs& a, bool one, int S, size_t stage, bool pdl, cudaStream_t st) {
+    if (S >= 2) {
+        const size_t smem = (size_t)kGemvWarps * S * stage;
+        return one ? launch_persistent(gateup_ring_kernel<CPL, true>, smem, pdl, st, a, S)
+                   : launch_persistent(gateup_ring_kernel<CPL, false>, smem, pdl, st, a, S);
+    }
+    return one ? launch_persistent(gateup_gemv_kernel<CPL, true>, 0, pdl, st, a)
+               : launch_persistent(gateup_gemv_kernel<CPL, false>, 0, pdl, st, a);
+}
+
+template <int CPL>
+cudaError_t launch_dn(const DnArgs& a, bool one, int S, size_t stage, int h_rows, bool pdl,
+                      cudaStream_t st) {
+    if (S >= 2) {
+        const size_t smem = (size_t)h_rows * a.ldh * 2 + (size_t)kGemvWarps * S * stage;
+        return one ? launch_persistent(down_ring_kernel<CPL, true>, smem, pdl, st, a, S, h_rows)
+                   : launch_persistent(down_ring_kernel<CPL, false>, smem, pdl, st, a, S, h_rows);
+    }
+    return one ? launch_persistent(down_gemv_kernel<CPL, true>, 0, pdl, st, a)
+               : launch_persistent(down_gemv_kernel<CPL, false>, 0, pdl, st, a);
+}
+
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
 }  // namespace
 
 cudaError_t launch_gateup_gemv(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,
                                const int32_t* perm, const int32_t* sched, moe_w4_t Wgu,
-                               moe_w4_t Wgu_s, uint16_t* H, WsHeader* hdr, cudaStream_t st) {
-    (void)hdr;
-    const int n_route = (int)std::min<int64_t>(d.E, (int64_t)d.T * d.k);
-    const int Fmax = std::max(d.F, d.F_s);
-    dim3 grid((Fmax + kGuRowsPerCta - 1) / kGuRowsPerCta, n_route + 1);
-    const size_t smem = (size_t)kGemvTok * d.d * 2;
-    cudaError_t err = ensure_dynamic_smem((const void*)gateup_gemv_kernel<kGemvTok>, smem);
-    if (err != cudaSuccess) return err;
-    gateup_gemv_kernel<kGemvTok><<<grid, 256, smem, st>>>(
-        x, d.T, d.d, d.k, d.F, d.F_s, d.group, offsets, perm, sched, Wgu.q,
-        reinterpret_cast<const __half*>(Wgu.s), Wgu_s.q, reinterpret_cast<const __half*>(Wgu_s.s),
-        H, Fmax, n_route);
-    return cudaGetLastError();
+                               moe_w4_t Wgu_s, uint16_t* H, const int32_t* n_active,
+                               WsHeader* hdr, bool pdl, cudaStream_t st) {
+    GuArgs a;
+    a.x = x;
+    a.T = d.T;
+    a.d = d.d;
+    a.k = d.k;
+    a.F = d.F;
+    a.Fs = d.F_s;
+    a.gsh = log2_group_chunks(d.group);
+    a.offsets = offsets;
+    a.perm = perm;
+    a.sched = sched;
+    a.q_r = Wgu.q;
+    a.s_r = reinterpret_cast<const __half*>(Wgu.s);
+    a.q_sh = Wgu_s.q;
+    a.s_sh = reinterpret_cast<const __half*>(Wgu_s.s);
+    a.H = H;
+    a.ldh = std::max(d.F, d.F_s);
+    a.n_route_max = (int)std::min<int64_t>(d.E, (int64_t)d.T * d.k);
+    a.n_active = n_active;
+    a.hdr = hdr;
+    const int cpl = chunks_per_lane(d.d, 4);
+    const bool single_pass = d.d / 32 <= 32 * cpl;
+    // the register-resident x form needs the whole row in one pass
+    const bool one = d.T == 1 && single_pass;
+    // ring: one stage holds a whole row pair, scale rows are 16-byte multiples
+    const int scb = d.d / d.group * 2;
+    const size_t stage = (size_t)d.d + 2 * scb;
+    const bool ring_ok = single_pass && scb % 16 == 0 && aligned16(Wgu.s) && aligned16(Wgu_s.s);
+    const int S = ring_ok ? ring_stages(stage) : 0;
+    switch (cpl) {
+        case 1: return launch_gu<1>(a, one, S, stage, pdl, st);
+        case 2: return launch_gu<2>(a, one, S, stage, pdl, st);
+        default: return launch_gu<4>(a, one, S, stage, pdl, st);
+    }
 }
 
 cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32_t* offsets,
                              const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y,
-                             WsHeader* hdr, cudaStream_t st) {
-    (void)hdr;
-    const int n_route = (int)std::min<int64_t>(d.E, (int64_t)d.T * d.k);
-    const int Fmax = std::max(d.F, d.F_s);
-    dim3 grid(d.d / kDnRowsPerCta, n_route + 1);
-    const size_t smem = (size_t)kGemvTok * Fmax * 2;
-    cudaError_t err = ensure_dynamic_smem((const void*)down_gemv_kernel<kGemvTok>, smem);
-    if (err != cudaSuccess) return err;
-    down_gemv_kernel<kGemvTok><<<grid, 256, smem, st>>>(
-        H, Fmax, d.T, d.d, d.k, d.F, d.F_s, d.group, offsets, sched, Wd.q,
-        reinterpret_cast<const __half*>(Wd.s), Wd_s.q, reinterpret_cast<const __half*>(Wd_s.s), Y,
-        n_route);
-    return cudaGetLastError();
+                             const int32_t* n_active, const float* topk_w, const int32_t* pos,
+                             uint16_t* out, WsHeader* hdr, bool pdl, cudaStream_t st) {
+    DnArgs a;
+    a.H = H;
+    a.ldh = std::max(d.F, d.F_s);
+    a.T = d.T;
+    a.d = d.d;
+    a.k = d.k;
+    a.F = d.F;
+    a.Fs = d.F_s;
+    a.gsh = log2_group_chunks(d.group);
+    a.offsets = offsets;
+    a.sched = sched;
+    a.q_r = Wd.q;
+    a.s_r = reinterpret_cast<const __half*>(Wd.s);
+    a.q_sh = Wd_s.q;
+    a.s_sh = reinterpret_cast<const __half*>(Wd_s.s);
+    a.Y = Y;
+    a.n_route_max = (int)std::min<int64_t>(d.E, (int64_t)d.T * d.k);
+    a.n_active = n_active;
+    a.topk_w = topk_w;
+    a.pos = pos;
+    a.out = out;
+    a.hdr = hdr;
+    const int Kmax = std::max(d.F, d.F_s);
+    const int cpl = chunks_per_lane(Kmax, 2);
+    const bool single_pass = Kmax / 32 <= 32 * cpl;
+    const bool one = d.T == 1;
+    // ring: one stage holds four whole rows; four scale rows are 16-byte multiples
+    const int sb_F = kDnQuad * (d.F / d.group) * 2, sb_Fs = kDnQuad * (d.F_s / d.group) * 2;
+    const size_t stage = (size_t)kDnQuad * (Kmax / 2) + kDnQuad * (Kmax / d.group) * 2;
+    const bool ring_ok = single_pass && sb_F % 16 == 0 && sb_Fs % 16 == 0 && aligned16(Wd.s) &&
+                         aligned16(Wd_s.s);
+    // a single token's H rows (k routed + 1 shared) are staged in shared memory
+    const size_t h_bytes = (size_t)(d.k + 1) * a.ldh * 2;
+    const int h_rows = (one && h_bytes <= kMaxStagedH) ? d.k + 1 : 0;
+    const int S = ring_ok ? ring_stages(stage, (size_t)h_rows * a.ldh * 2) : 0;
+    return cpl == 1 ? launch_dn<1>(a, one, S, stage, h_rows, pdl, st)
+                    : launch_dn<2>(a, one, S, stage, h_rows, pdl, st);
 }
 
 }  // namespace moe

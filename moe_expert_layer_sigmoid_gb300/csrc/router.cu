@@ -9,70 +9,23 @@
 // a warp-per-token kernel that sums the partials in a fixed order, applies the
 // sigmoid and the bias, and extracts the top k by k rounds of a warp shuffle
 // arg-max (ties to the lower expert id).
-#include <cfloat>
-
-#include "common.cuh"
+#include "router_dev.cuh"
 
 namespace moe {
 namespace {
 
 // ---------------------------------------------------------------------------
 // Small T (decode): split-K GEMV.  Grid (E / 8, ksplit); warp w of block b owns
-// expert 8b + w over K range [kc * kchunk, (kc + 1) * kchunk) and every token.
-// W_r is read once, with 16-byte coalesced loads spread over E/8 * ksplit CTAs.
-constexpr int kRouterTokTile = 16;
-
+// expert 8b + w over one K range and every token.  W_r is read once, with
+// 16-byte coalesced loads spread over E/8 * ksplit CTAs.
 __global__ void __launch_bounds__(256) router_logits_gemv(const uint16_t* __restrict__ x,
                                                          const float* __restrict__ W_r, int T,
                                                          int d, int E, int kchunk,
                                                          float* __restrict__ partial) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * 8 + warp;
-    const int kc = blockIdx.y;
     if (e >= E) return;
-    const int k0 = kc * kchunk;
-    const int nvec = kchunk / 128;  // float4 loads per lane (kchunk in {256, 512})
-    // this lane's W_r slice: float4 at k0 + 4 * (lane + 32 * i)
-    float4 wv[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if (i < nvec)
-            wv[i] = __ldg(reinterpret_cast<const float4*>(W_r + (int64_t)e * d + k0) + lane + 32 * i);
-        else
-            wv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int t0 = 0; t0 < T; t0 += kRouterTokTile) {
-        float acc[kRouterTokTile];
-#pragma unroll
-        for (int tt = 0; tt < kRouterTokTile; ++tt) acc[tt] = 0.f;
-#pragma unroll
-        for (int tt = 0; tt < kRouterTokTile; ++tt) {
-            const int t = t0 + tt;
-            if (t < T) {
-                const uint2* xr = reinterpret_cast<const uint2*>(x + (int64_t)t * d + k0);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (i < nvec) {
-                        uint2 xv = __ldg(xr + lane + 32 * i);
-                        float a = acc[tt];
-                        a = fmaf(bf16_lo(xv.x), wv[i].x, a);
-                        a = fmaf(bf16_hi(xv.x), wv[i].y, a);
-                        a = fmaf(bf16_lo(xv.y), wv[i].z, a);
-                        a = fmaf(bf16_hi(xv.y), wv[i].w, a);
-                        acc[tt] = a;
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int tt = 0; tt < kRouterTokTile; ++tt) {
-            float v = acc[tt];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            const int t = t0 + tt;
-            if (lane == 0 && t < T) partial[((int64_t)kc * T + t) * E + e] = v;
-        }
-    }
+    router_gemv_warp(x, W_r, T, d, E, e, blockIdx.y, kchunk, partial, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -132,29 +85,7 @@ __global__ void __launch_bounds__(256) router_logits_sgemm(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------------------
-// Top-k: one warp per token; lane l holds experts l, l + 32, ...
-struct Cand {
-    float key;
-    float s;
-    int e;
-};
-
-__device__ __forceinline__ bool better(float ka, int ea, float kb, int eb) {
-    return ka > kb || (ka == kb && ea < eb);
-}
-
-__device__ __forceinline__ Cand warp_argmax(Cand c) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        Cand o_c;
-        o_c.key = __shfl_xor_sync(0xffffffffu, c.key, o);
-        o_c.s = __shfl_xor_sync(0xffffffffu, c.s, o);
-        o_c.e = __shfl_xor_sync(0xffffffffu, c.e, o);
-        if (better(o_c.key, o_c.e, c.key, c.e)) c = o_c;
-    }
-    return c;
-}
-
+// Top-k: one warp per token.
 template <int NV>
 __global__ void __launch_bounds__(256) router_topk(const float* __restrict__ partial, int ksplit,
                                                   const float* __restrict__ bias, int T, int E,
@@ -164,58 +95,8 @@ __global__ void __launch_bounds__(256) router_topk(const float* __restrict__ par
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
-    float key[NV], sv[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            float l = 0.f;
-            for (int kc = 0; kc < ksplit; ++kc) l += partial[((int64_t)kc * T + t) * E + e];
-            const float s = 1.0f / (1.0f + expf(-l));
-            sv[i] = s;
-            key[i] = s + __ldg(bias + e);
-        } else {
-            sv[i] = 0.f;
-            key[i] = -FLT_MAX;
-        }
-    }
-    int my_e = -1;
-    float my_s = 0.f, kth_key = 0.f;
-    for (int j = 0; j < k; ++j) {
-        Cand c{-INFINITY, 0.f, 0x7fffffff};
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && key[i] != -INFINITY && better(key[i], e, c.key, c.e)) c = Cand{key[i], sv[i], e};
-        }
-        c = warp_argmax(c);
-        if (lane == j) { my_e = c.e; my_s = c.s; }
-        kth_key = c.key;
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (lane + 32 * i == c.e) key[i] = -INFINITY;
-    }
-    if (margin) {
-        float m = INFINITY;
-        if (k < E) {
-            Cand c{-INFINITY, 0.f, 0x7fffffff};
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && key[i] != -INFINITY && better(key[i], e, c.key, c.e)) c = Cand{key[i], sv[i], e};
-            }
-            c = warp_argmax(c);
-            m = kth_key - c.key;
-        }
-        if (lane == 0) margin[t] = m;
-    }
-    // normaliser: sum of the selected scores in selection order
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, my_s, j);
-    if (lane < k) {
-        topk_idx[(int64_t)t * k + lane] = my_e;
-        topk_w[(int64_t)t * k + lane] = __fdiv_rn(my_s, sum);
-    }
+    int sel;
+    router_topk_warp<NV>(partial, ksplit, bias, T, E, k, t, lane, topk_idx, topk_w, margin, &sel);
 }
 
 }  // namespace
