@@ -131,6 +131,117 @@ __device__ __forceinline__ void topk_rank_block(const DecodeRouterArgs& a, int k
     __syncthreads();
 }
 
+// Bitonic sort of one (key, e, v) per lane across a warp.  DESC: best first
+// by (key, then lower e); otherwise by ascending e alone.
+template <bool DESC>
+__device__ __forceinline__ void warp_bitonic(float& key, int& e, float& v, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float pk = __shfl_xor_sync(0xffffffffu, key, stride);
+            const int pe = __shfl_xor_sync(0xffffffffu, e, stride);
+            const float pv = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool partner_first = DESC ? router_better(pk, pe, key, e) : pe < e;
+            const bool lower = (lane & stride) == 0;
+            const bool dir = (lane & size) == 0;  // this run is sorted first-to-last
+            if (lower == dir ? partner_first : !partner_first) {
+                key = pk;
+                e = pe;
+                v = pv;
+            }
+        }
+    }
+}
+
+// Single token, E <= 256: one expert per thread.  Each warp sorts its 32 keys
+// and keeps its best k + 1 as candidates; a candidate's rank among all
+// candidates is its rank among all experts (an expert outside its warp's best
+// k + 1 has rank above k).  The descriptors of one token follow directly:
+// the k chosen experts have one row each, in id order.
+__device__ __forceinline__ void decode_route_one(const DecodeRouterArgs& a, int ksplit,
+                                                 float* s_ckey, float* s_cs, int32_t* s_ce,
+                                                 int* s_sel_e, float* s_sel_s, float* s_gap) {
+    const int E = a.E, k = a.k;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nc = min(k + 1, 32);  // candidates per warp
+    {
+        const int e = tid;
+        float key = -INFINITY, sc = 0.f;
+        int ee = 0x7fffffff;
+        if (e < E) {
+            const float l = router_logit(a.partial, ksplit, 1, E, 0, e);
+            sc = 1.0f / (1.0f + expf(-l));
+            key = sc + __ldg(a.bias + e);
+            if (key != key) key = -INFINITY;
+            ee = e;
+        }
+        warp_bitonic<true>(key, ee, sc, lane);
+        if (lane < nc) {
+            s_ckey[warp * nc + lane] = key;
+            s_ce[warp * nc + lane] = ee;
+            s_cs[warp * nc + lane] = sc;
+        }
+    }
+    __syncthreads();
+    const int ncand = nc * (kRouterThreads / 32);
+    if (tid < ncand) {
+        const float key = s_ckey[tid];
+        const int e = s_ce[tid];
+        if (e < E) {
+            int rank = 0;
+            for (int j = 0; j < ncand; ++j) {
+                const int e2 = s_ce[j];
+                rank += e2 < E && router_better(s_ckey[j], e2, key, e);
+            }
+            if (rank < k) {
+                s_sel_e[rank] = e;
+                s_sel_s[rank] = s_cs[tid];
+            }
+            if (rank == k - 1) s_gap[0] = key;
+            if (rank == k) s_gap[1] = key;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // outputs of the selection, then the chosen ids sorted ascending with
+        // their slots: row r of the descriptors is the r-th smallest id
+        float sum = 0.f;
+        for (int r = 0; r < k; ++r) sum += s_sel_s[r];
+        int e = 0x7fffffff;
+        float slot = 0.f;
+        if (lane < k) {
+            e = s_sel_e[lane];
+            a.topk_idx[lane] = e;
+            a.topk_w[lane] = __fdiv_rn(s_sel_s[lane], sum);
+            slot = (float)lane;
+        }
+        if (a.margin && lane == 0) a.margin[0] = k < E ? s_gap[0] - s_gap[1] : INFINITY;
+        float dummy = 0.f;
+        warp_bitonic<false>(dummy, e, slot, lane);
+        if (lane < k) {
+            const int j = (int)slot;
+            a.perm[lane] = j;
+            a.pos[j] = lane;
+            a.sched[lane] = e;
+            s_ce[lane] = e;  // sorted ids for the per-expert pass
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kRouterThreads) {
+        int lb = 0;  // chosen ids below e
+        while (lb < k && s_ce[lb] < e) ++lb;
+        const bool chosen = lb < k && s_ce[lb] == e;
+        a.counts[e] = chosen ? 1 : 0;
+        a.offsets[e] = lb;
+        if (!chosen) a.sched[k + (e - lb)] = e;
+    }
+    if (tid == 0) {
+        a.offsets[E] = k;
+        a.hdr->n_active = k;
+    }
+}
+
 template <int NV>
 __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(const DecodeRouterArgs a) {
     __shared__ int32_t s_idx[kMaxDecodeT * kMaxDecodeK];
@@ -163,6 +274,11 @@ __global__ void __launch_bounds__(kRouterThreads) router_decode_kernel(const Dec
     if (!s_last) return;
     __threadfence();
     if (tid == 0) a.hdr->done[0] = 0;  // every CTA has arrived: ready for the next launch
+
+    if (T == 1 && E <= kRouterThreads) {
+        decode_route_one(a, gridDim.y, s_key, s_sc, s_act, s_sel_e, s_sel_s, s_gap);
+        return;
+    }
 
     // ---- top-k: few tokens by rank counting over the whole CTA, more tokens
     // one warp per token

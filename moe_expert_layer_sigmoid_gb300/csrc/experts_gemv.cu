@@ -47,8 +47,15 @@
 namespace moe {
 namespace {
 
-constexpr int kGemvWarps = 16;
-constexpr int kGemvThreads = kGemvWarps * 32;
+// Gate+up: 8 warps at up to 128 registers (32K of the 64K-register file) and
+// a 135 KB ring, so a CTA fits beside the decode router's last CTA and every
+// CTA is resident (and stages its shared-expert rows) when the routing lands.
+// Down: 16 warps.
+constexpr int kGuWarps = 8;
+constexpr int kGuRP = 2;  // row pairs per ring unit of the gate+up kernel
+constexpr int kGuThreads = kGuWarps * 32;
+constexpr int kDnWarps = 16;
+constexpr int kDnThreads = kDnWarps * 32;
 constexpr int kGuTokPass = 4;  // tokens per pass of the gate+up kernel (T > 1)
 constexpr int kDnTokPass = 2;  // tokens per pass of the down kernel (T > 1)
 constexpr int kDnQuad = 4;     // output channels per down work item
@@ -162,6 +169,20 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Sums of four per-lane values over the warp, transposed: lane L ends with the
+// total of value ((L >> 4) & 1) * 2 + ((L >> 3) & 1), in 7 shuffles.
+__device__ __forceinline__ float reduce4(float v0, float v1, float v2, float v3, int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8;
+    const float a = (h16 ? v0 : v2) + 0.f, b = (h16 ? v1 : v3) + 0.f;
+    const float w0 = (h16 ? v2 : v0) + __shfl_xor_sync(0xffffffffu, a, 16);
+    const float w1 = (h16 ? v3 : v1) + __shfl_xor_sync(0xffffffffu, b, 16);
+    float z = (h8 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, h8 ? w0 : w1, 8);
+    z += __shfl_xor_sync(0xffffffffu, z, 4);
+    z += __shfl_xor_sync(0xffffffffu, z, 2);
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+    return z;
+}
+
 __device__ __forceinline__ void load_chunk(const uint16_t* row, int c, uint4* xv) {
     const uint4* p = reinterpret_cast<const uint4*>(row) + 4 * c;
 #pragma unroll
@@ -190,7 +211,8 @@ __device__ __forceinline__ int active_groups(const int32_t* n_active, const int3
 
 // ---------------------------------------------------------------------------
 constexpr int kMaxRing = 6;                     // stages per warp, at most
-constexpr int kRingSmemBudget = 200 * 1024;     // dynamic shared memory of a ring kernel
+constexpr int kGuRingBudget = 152 * 1024;       // dynamic shared memory of the gate+up ring
+constexpr int kDnRingBudget = 200 * 1024;       // dynamic shared memory of the down ring
 constexpr size_t kMaxStagedH = 64 * 1024;       // H rows staged by the down kernel, at most
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -198,6 +220,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 __device__ __forceinline__ float lds_f16(uint32_t addr) {
@@ -381,7 +408,7 @@ __device__ __forceinline__ void gu_routed_item(const GuArgs& a, int64_t it, int*
 
 // Load path.
 template <int CPL, bool ONE>
-__global__ void __launch_bounds__(kGemvThreads, 1) gateup_gemv_kernel(const GuArgs a) {
+__global__ void __maxnreg__(128) gateup_gemv_kernel(const GuArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, b = blockIdx.x;
     uint4 xr[CPL][4];
@@ -390,7 +417,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gateup_gemv_kernel(const GuAr
     // the shared expert reads only x: it runs before the wait for the router
     {
         const int lo = (int)((int64_t)b * a.Fs / G), hi = (int)((int64_t)(b + 1) * a.Fs / G);
-        for (int f = lo + warp; f < hi; f += kGemvWarps) {
+        for (int f = lo + warp; f < hi; f += kGuWarps) {
             int row0, count;
             group_rows(a.offsets, a.T, a.k, -1, &row0, &count);
             gu_compute<CPL, ONE, false>(a, -1, f, gu_rows_global(a, -1, f), row0, count, xr, xs, lane);
@@ -401,7 +428,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gateup_gemv_kernel(const GuAr
     const int n_act = active_groups(a.n_active, a.offsets, a.sched, a.n_route_max);
     const int64_t R = (int64_t)n_act * a.F;
     const int64_t lo = (int64_t)b * R / G, hi = (int64_t)(b + 1) * R / G;
-    for (int64_t it = lo + warp; it < hi; it += kGemvWarps) {
+    for (int64_t it = lo + warp; it < hi; it += kGuWarps) {
         int e, f, row0, count;
         gu_routed_item(a, it, &e, &f);
         group_rows(a.offsets, a.T, a.k, e, &row0, &count);
@@ -409,54 +436,163 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gateup_gemv_kernel(const GuAr
     }
 }
 
-// Ring path.  Stage of one item: [gate q | up q | gate scales | up scales].
+// One ring unit of the gate+up kernel: row pairs f0 .. f0 + kGuRP - 1 of
+// `expert` (-1: shared) from a stage laid out as [gate q rows | up q rows |
+// gate scale rows | up scale rows], against the group's rows [row0, row0 +
+// count), writing SwiGLU(gate, up) to H.
 template <int CPL, bool ONE>
-__global__ void __launch_bounds__(kGemvThreads, 1) gateup_ring_kernel(const GuArgs a, int S) {
+__device__ __forceinline__ void gu_unit(const GuArgs& a, int expert, int f0, uint32_t st,
+                                        int row0, int count, const uint4 (&xr)[CPL][4],
+                                        const float (&xs)[CPL], int lane) {
+    static_assert(kGuRP == 2, "the reduction below pairs two row pairs");
+    const int nc = a.d >> 5;
+    const uint32_t rowb = (uint32_t)(a.d / 2), scb = (uint32_t)(((a.d >> 5) >> a.gsh) * 2);
+    RowRef rg[kGuRP], ru[kGuRP];
+#pragma unroll
+    for (int r = 0; r < kGuRP; ++r) {
+        rg[r].q = ru[r].q = nullptr;
+        rg[r].s = ru[r].s = nullptr;
+        rg[r].sq = st + r * rowb;
+        ru[r].sq = st + (kGuRP + r) * rowb;
+        rg[r].ss = st + 2 * kGuRP * rowb + r * scb;
+        ru[r].ss = st + 2 * kGuRP * rowb + (kGuRP + r) * scb;
+    }
+    if constexpr (ONE) {
+        float g[kGuRP], u[kGuRP];
+#pragma unroll
+        for (int r = 0; r < kGuRP; ++r) g[r] = u[r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int c = lane + 32 * i;
+            if (c < nc) {
+#pragma unroll
+                for (int r = 0; r < kGuRP; ++r) {
+                    const uint4 wg = row_word<true>(rg[r], c), wu = row_word<true>(ru[r], c);
+                    const float sg = row_scale<true>(rg[r], c >> a.gsh);
+                    const float su = row_scale<true>(ru[r], c >> a.gsh);
+                    g[r] = fmaf(sg, fmaf(-136.f, xs[i], dot32_off(wg, xr[i])), g[r]);
+                    u[r] = fmaf(su, fmaf(-136.f, xs[i], dot32_off(wu, xr[i])), u[r]);
+                }
+            }
+        }
+        // lanes 0 / 8 / 16 / 24 hold gate 0 / up 0 / gate 1 / up 1
+        const float z = reduce4(g[0], u[0], g[1], u[1], lane);
+        const float zu = __shfl_down_sync(0xffffffffu, z, 8);
+        if ((lane & 15) == 0 && count > 0)
+            a.H[(int64_t)row0 * a.ldh + f0 + (lane >> 4)] = float_to_bf16_bits(swiglu(z, zu));
+    } else {
+        for (int i0 = 0; i0 < count; i0 += kGuTokPass) {
+            const int ntok = min(kGuTokPass, count - i0);
+            const uint16_t* xrow[kGuTokPass];
+#pragma unroll
+            for (int tt = 0; tt < kGuTokPass; ++tt) {
+                const int r = row0 + i0 + min(tt, ntok - 1);
+                const int tok = expert >= 0 ? a.perm[r] / a.k : r - row0;
+                xrow[tt] = a.x + (int64_t)tok * a.d;
+            }
+            float g[kGuTokPass][kGuRP], u[kGuTokPass][kGuRP];
+#pragma unroll
+            for (int tt = 0; tt < kGuTokPass; ++tt)
+#pragma unroll
+                for (int r = 0; r < kGuRP; ++r) g[tt][r] = u[tt][r] = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                const int c = lane + 32 * i;
+                if (c >= nc) continue;
+#pragma unroll
+                for (int r = 0; r < kGuRP; ++r) {
+                    uint32_t qg[16], qu[16];
+                    q_pairs32(row_word<true>(rg[r], c), qg);
+                    q_pairs32(row_word<true>(ru[r], c), qu);
+                    const float sg = row_scale<true>(rg[r], c >> a.gsh);
+                    const float su = row_scale<true>(ru[r], c >> a.gsh);
+#pragma unroll
+                    for (int tt = 0; tt < kGuTokPass; ++tt) {
+                        if (tt < ntok) {
+                            uint4 xv[4];
+                            load_chunk(xrow[tt], c, xv);
+                            g[tt][r] = fmaf(sg, dot32_q(qg, xv), g[tt][r]);
+                            u[tt][r] = fmaf(su, dot32_q(qu, xv), u[tt][r]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int tt = 0; tt < kGuTokPass; ++tt) {
+                if (tt < ntok) {
+                    const float z = reduce4(g[tt][0], u[tt][0], g[tt][1], u[tt][1], lane);
+                    const float zu = __shfl_down_sync(0xffffffffu, z, 8);
+                    if ((lane & 15) == 0)
+                        a.H[(int64_t)(row0 + i0 + tt) * a.ldh + f0 + (lane >> 4)] =
+                            float_to_bf16_bits(swiglu(z, zu));
+                }
+            }
+        }
+    }
+}
+
+// Ring path.  A unit is kGuRP consecutive row pairs of one group; its stage
+// holds [gate q rows | up q rows | gate scale rows | up scale rows].
+template <int CPL, bool ONE>
+__global__ void __maxnreg__(128) gateup_ring_kernel(const GuArgs a, int S) {
     extern __shared__ __align__(128) uint8_t ring_smem[];
-    __shared__ __align__(8) uint64_t s_bar[kGemvWarps * kMaxRing];
+    __shared__ __align__(8) uint64_t s_bar[kGuWarps * kMaxRing];
     __shared__ int s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, b = blockIdx.x;
     const int64_t rowb = a.d / 2;
     const int scb = ((a.d >> 5) >> a.gsh) * 2;
-    const uint32_t stage_bytes = (uint32_t)(2 * rowb + 2 * scb);
+    const uint32_t stage_bytes = (uint32_t)(kGuRP * (2 * rowb + 2 * scb));
     uint8_t* wbuf = ring_smem + (size_t)warp * S * stage_bytes;
     const uint32_t bar0 = smem_u32(&s_bar[warp * kMaxRing]);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kGemvWarps * kMaxRing; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
+        for (int i = 0; i < kGuWarps * kMaxRing; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    // Units of this warp, in order: its shared-expert items, then its routed
-    // items.  The shared expert depends on x alone, so its first stages are
+    // Units of this warp, in order: its shared-expert units, then its routed
+    // units.  The shared expert depends on x alone, so its first stages are
     // requested before the wait for the router; nothing routed is touched
-    // before that wait.
-    const int64_t s_first = (int64_t)b * a.Fs / G + warp, s_hi = (int64_t)(b + 1) * a.Fs / G;
-    const int n_sh = s_first < s_hi ? (int)((s_hi - s_first + kGemvWarps - 1) / kGemvWarps) : 0;
-    int64_t r_first = 0;
+    // before that wait.  Routed units are walked with cursors (group, unit),
+    // one for the stages being requested and one for the stages being used.
+    const int Fu = a.F / kGuRP, Fsu = a.Fs / kGuRP;  // units per group
+    const int s_first = (int)((int64_t)b * Fsu / G) + warp, s_hi = (int)((int64_t)(b + 1) * Fsu / G);
+    const int n_sh = s_first < s_hi ? (s_hi - s_first + kGuWarps - 1) / kGuWarps : 0;
     int n_units = n_sh;
-    auto item = [&](int u, int* e, int* f) {
+    struct Cursor {
+        int y, j;
+    };
+    Cursor pc{0, 0}, cc{0, 0};  // producer (lane 0) and consumer cursors
+    // expert and first row pair of unit u; routed units advance the cursor
+    auto item = [&](int u, Cursor& c, int* e, int* f0) {
         if (u < n_sh) {
             *e = -1;
-            *f = (int)(s_first + (int64_t)u * kGemvWarps);
+            *f0 = kGuRP * (s_first + u * kGuWarps);
         } else {
-            gu_routed_item(a, r_first + (int64_t)(u - n_sh) * kGemvWarps, e, f);
+            *e = a.sched[c.y];
+            *f0 = kGuRP * c.j;
+            c.j += kGuWarps;
+            while (c.j >= Fu) {
+                c.j -= Fu;
+                ++c.y;
+            }
         }
     };
     auto issue = [&](int u) {  // lane 0
-        int e, f;
-        item(u, &e, &f);
-        const GuRows g = gu_rows_global(a, e, f);
+        int e, f0;
+        item(u, pc, &e, &f0);
+        const GuRows g = gu_rows_global(a, e, f0);
         const uint32_t slot = u % S;
         const uint32_t dst = smem_u32(wbuf + slot * stage_bytes);
         const uint32_t bar = bar0 + 8 * slot;
+        const uint32_t qb = (uint32_t)(kGuRP * rowb), sb = (uint32_t)(kGuRP * scb);
         mbar_expect_tx(bar, stage_bytes);
-        bulk_load(dst, g.g.q, (uint32_t)rowb, bar);
-        bulk_load(dst + (uint32_t)rowb, g.u.q, (uint32_t)rowb, bar);
-        bulk_load(dst + 2 * (uint32_t)rowb, g.g.s, scb, bar);
-        bulk_load(dst + 2 * (uint32_t)rowb + scb, g.u.s, scb, bar);
+        bulk_load(dst, g.g.q, qb, bar);
+        bulk_load(dst + qb, g.u.q, qb, bar);
+        bulk_load(dst + 2 * qb, g.g.s, sb, bar);
+        bulk_load(dst + 2 * qb + sb, g.u.s, sb, bar);
     };
     if (lane == 0)
         for (int u = 0; u < n_sh && u < S; ++u) issue(u);
@@ -471,28 +607,24 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gateup_ring_kernel(const GuAr
     pdl_trigger();
     const int n_act = active_groups(a.n_active, a.offsets, a.sched, a.n_route_max);
     {
-        const int64_t R = (int64_t)n_act * a.F;
+        const int64_t R = (int64_t)n_act * Fu;
         const int64_t lo = (int64_t)b * R / G, hi = (int64_t)(b + 1) * R / G;
-        r_first = lo + warp;
-        n_units += r_first < hi ? (int)((hi - r_first + kGemvWarps - 1) / kGemvWarps) : 0;
+        const int64_t r_first = lo + warp;
+        if (r_first < hi) {
+            n_units += (int)((hi - r_first + kGuWarps - 1) / kGuWarps);
+            pc.y = cc.y = (int)(r_first / Fu);
+            pc.j = cc.j = (int)(r_first - (int64_t)pc.y * Fu);
+        }
     }
     if (lane == 0)
         for (int u = n_sh; u < n_units && u < S; ++u) issue(u);
     for (int u = 0; u < n_units; ++u) {
         const uint32_t slot = u % S;
         if (!mbar_wait(bar0 + 8 * slot, (u / S) & 1, &s_abort, a.hdr)) return;
-        int e, f, row0, count;
-        item(u, &e, &f);
+        int e, f0, row0, count;
+        item(u, cc, &e, &f0);
         group_rows(a.offsets, a.T, a.k, e, &row0, &count);
-        const uint32_t st = smem_u32(wbuf + slot * stage_bytes);
-        GuRows w;
-        w.g.q = w.u.q = nullptr;
-        w.g.s = w.u.s = nullptr;
-        w.g.sq = st;
-        w.u.sq = st + (uint32_t)rowb;
-        w.g.ss = st + 2 * (uint32_t)rowb;
-        w.u.ss = st + 2 * (uint32_t)rowb + scb;
-        gu_compute<CPL, ONE, true>(a, e, f, w, row0, count, xr, xs, lane);
+        gu_unit<CPL, ONE>(a, e, f0, smem_u32(wbuf + slot * stage_bytes), row0, count, xr, xs, lane);
         __syncwarp();
         if (lane == 0 && u + S < n_units) {
             fence_proxy_async_smem();  // the stage was read with plain loads
@@ -554,10 +686,11 @@ __device__ __forceinline__ RowRef dn_channel(const DnRows& w, int ch, int64_t ro
 // One down item: channels c0 .. c0 + 3 of `expert` (-1: shared) for the
 // group's rows [row0, row0 + count), writing Y.
 // hs (ONE only): shared-memory address of the staged H rows (0: read H from
-// global memory).
+// global memory); hsum: their 32-element chunk sums, [row][K / 32] fp32.
 template <int CPL, bool ONE, bool SMEM>
 __device__ __forceinline__ void dn_compute(const DnArgs& a, int expert, int c0, const DnRows& w,
-                                           int row0, int count, int lane, uint32_t hs = 0) {
+                                           int row0, int count, int lane, uint32_t hs = 0,
+                                           uint32_t hsum = 0) {
     const int K = expert >= 0 ? a.F : a.Fs;
     const int nc = K >> 5, ngr = nc >> a.gsh;
     const int64_t rowb = K / 2;
@@ -576,20 +709,22 @@ __device__ __forceinline__ void dn_compute(const DnArgs& a, int expert, int c0, 
                 if (c >= nc) continue;
                 if constexpr (ONE) {
                     uint4 hv[4];
+                    float hsm;
                     if (hs) {
                         const uint32_t h = hs + (uint32_t)(row0 * a.ldh + 32 * c) * 2u;
 #pragma unroll
                         for (int v = 0; v < 4; ++v) hv[v] = lds128(h + 16u * v);
+                        hsm = lds_f32(hsum + 4u * (uint32_t)(row0 * (a.ldh >> 5) + c));
                     } else {
                         load_chunk(a.H + (int64_t)row0 * a.ldh, c, hv);
+                        hsm = sum32_bf16(hv);
                     }
-                    const float hs = sum32_bf16(hv);
 #pragma unroll
                     for (int ch = 0; ch < kDnQuad; ++ch) {
                         const RowRef r = dn_channel(w, ch, rowb, ngr);
                         const uint4 wq = row_word<SMEM>(r, c);
                         const float sc = row_scale<SMEM>(r, c >> a.gsh);
-                        const float p = fmaf(-136.f, hs, dot32_off(wq, hv));
+                        const float p = fmaf(-136.f, hsm, dot32_off(wq, hv));
                         acc[0][ch] = fmaf(sc, p, acc[0][ch]);
                     }
                 } else {
@@ -613,13 +748,9 @@ __device__ __forceinline__ void dn_compute(const DnArgs& a, int expert, int c0, 
 #pragma unroll
         for (int tt = 0; tt < TP; ++tt) {
             if (tt < ntok) {
-                float4 v;
-                v.x = warp_sum(acc[tt][0]);
-                v.y = warp_sum(acc[tt][1]);
-                v.z = warp_sum(acc[tt][2]);
-                v.w = warp_sum(acc[tt][3]);
-                if (lane == 0)
-                    *reinterpret_cast<float4*>(a.Y + (int64_t)(row0 + i0 + tt) * a.d + c0) = v;
+                // lanes 0 / 8 / 16 / 24 hold channels c0 .. c0 + 3
+                const float z = reduce4(acc[tt][0], acc[tt][1], acc[tt][2], acc[tt][3], lane);
+                if ((lane & 7) == 0) a.Y[(int64_t)(row0 + i0 + tt) * a.d + c0 + (lane >> 3)] = z;
             }
         }
     }
@@ -674,7 +805,7 @@ __device__ __forceinline__ void dn_combine(const DnArgs& a, int q_lo, int nqc) {
 
 // Load path.
 template <int CPL, bool ONE>
-__global__ void __launch_bounds__(kGemvThreads, 1) down_gemv_kernel(const DnArgs a) {
+__global__ void __launch_bounds__(kDnThreads, 1) down_gemv_kernel(const DnArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int q_lo, q_hi;
     dn_share(a.d, &q_lo, &q_hi);
@@ -683,7 +814,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) down_gemv_kernel(const DnArgs
     pdl_wait();
     const int n_act = active_groups(a.n_active, a.offsets, a.sched, a.n_route_max);
     const int items = (1 + n_act) * nqc;
-    for (int it = warp; it < items; it += kGemvWarps) {
+    for (int it = warp; it < items; it += kDnWarps) {
         int e, c0, row0, count;
         dn_item(a, it, nqc, q_lo, &e, &c0);
         group_rows(a.offsets, a.T, a.k, e, &row0, &count);
@@ -696,20 +827,21 @@ __global__ void __launch_bounds__(kGemvThreads, 1) down_gemv_kernel(const DnArgs
 // of the widest group (max(F, F_s)).  Shared memory: [H rows (h_rows of ldh,
 // T == 1 only) | per-warp rings].
 template <int CPL, bool ONE>
-__global__ void __launch_bounds__(kGemvThreads, 1) down_ring_kernel(const DnArgs a, int S,
+__global__ void __launch_bounds__(kDnThreads, 1) down_ring_kernel(const DnArgs a, int S,
                                                                     int h_rows) {
     extern __shared__ __align__(128) uint8_t ring_smem[];
-    __shared__ __align__(8) uint64_t s_bar[kGemvWarps * kMaxRing];
+    __shared__ __align__(8) uint64_t s_bar[kDnWarps * kMaxRing];
     __shared__ int s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Kmax = max(a.F, a.Fs);
     const uint32_t q_bytes = (uint32_t)(kDnQuad * (Kmax / 2));
     const uint32_t stage_bytes = q_bytes + (uint32_t)(kDnQuad * (((Kmax >> 5) >> a.gsh) * 2));
     const uint32_t h_bytes = (uint32_t)h_rows * a.ldh * 2u;
-    uint8_t* wbuf = ring_smem + h_bytes + (size_t)warp * S * stage_bytes;
+    const uint32_t hsum_bytes = (uint32_t)h_rows * (a.ldh >> 5) * 4u;
+    uint8_t* wbuf = ring_smem + h_bytes + hsum_bytes + (size_t)warp * S * stage_bytes;
     const uint32_t bar0 = smem_u32(&s_bar[warp * kMaxRing]);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kGemvWarps * kMaxRing; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
+        for (int i = 0; i < kDnWarps * kMaxRing; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -723,10 +855,25 @@ __global__ void __launch_bounds__(kGemvThreads, 1) down_ring_kernel(const DnArgs
     // requested now, and only H (written by the gate+up kernel) waits.
     const int n_act = active_groups(a.n_active, a.offsets, a.sched, a.n_route_max);
     const int items = (1 + n_act) * nqc;
-    const int n = warp < items ? (items - warp + kGemvWarps - 1) / kGemvWarps : 0;
+    const int n = warp < items ? (items - warp + kDnWarps - 1) / kDnWarps : 0;
+    // items walked with cursors (group, quad): producer (lane 0) and consumer
+    struct Cursor {
+        int y, qd;
+    };
+    Cursor pc{0, 0}, cc{0, 0};
+    if (n) pc.y = cc.y = warp / nqc, pc.qd = cc.qd = warp - (warp / nqc) * nqc;
+    auto item = [&](Cursor& c, int* e, int* c0) {
+        *e = c.y == 0 ? -1 : a.sched[c.y - 1];
+        *c0 = kDnQuad * (q_lo + c.qd);
+        c.qd += kDnWarps;
+        while (c.qd >= nqc) {
+            c.qd -= nqc;
+            ++c.y;
+        }
+    };
     auto issue = [&](int u) {  // lane 0
         int e, c0;
-        dn_item(a, warp + u * kGemvWarps, nqc, q_lo, &e, &c0);
+        item(pc, &e, &c0);
         const DnRows g = dn_rows_global(a, e, c0);
         const int K = e >= 0 ? a.F : a.Fs;
         const uint32_t qb = (uint32_t)(kDnQuad * (K / 2));
@@ -741,26 +888,31 @@ __global__ void __launch_bounds__(kGemvThreads, 1) down_ring_kernel(const DnArgs
     if (lane == 0)
         for (int u = 0; u < n && u < S; ++u) issue(u);
     pdl_wait();
-    uint32_t hs = 0;
-    if (h_rows) {  // H rows of a single token, staged once for every item
+    uint32_t hs = 0, hsum = 0;
+    if (h_rows) {  // H rows of a single token and their chunk sums, staged once
         const uint4* src = reinterpret_cast<const uint4*>(a.H);
         uint4* dst = reinterpret_cast<uint4*>(ring_smem);
-        for (uint32_t i = threadIdx.x; i < h_bytes / 16; i += kGemvThreads) dst[i] = __ldg(src + i);
+        for (uint32_t i = threadIdx.x; i < h_bytes / 16; i += kDnThreads) dst[i] = __ldg(src + i);
+        __syncthreads();
+        const int ncr = a.ldh >> 5;  // chunks per row
+        float* sums = reinterpret_cast<float*>(ring_smem + h_bytes);
+        for (int i = threadIdx.x; i < h_rows * ncr; i += kDnThreads) sums[i] = sum32_bf16(dst + 4 * i);
         __syncthreads();
         hs = smem_u32(ring_smem);
+        hsum = smem_u32(sums);
     }
     for (int u = 0; u < n; ++u) {
         const uint32_t slot = u % S;
         if (!mbar_wait(bar0 + 8 * slot, (u / S) & 1, &s_abort, a.hdr)) break;
         int e, c0, row0, count;
-        dn_item(a, warp + u * kGemvWarps, nqc, q_lo, &e, &c0);
+        item(cc, &e, &c0);
         group_rows(a.offsets, a.T, a.k, e, &row0, &count);
         DnRows w;
         w.q = nullptr;
         w.s = nullptr;
         w.sq = smem_u32(wbuf + slot * stage_bytes);
         w.ss = w.sq + q_bytes;
-        dn_compute<CPL, ONE, true>(a, e, c0, w, row0, count, lane, hs);
+        dn_compute<CPL, ONE, true>(a, e, c0, w, row0, count, lane, hs, hsum);
         __syncwarp();
         if (lane == 0 && u + S < n) {
             fence_proxy_async_smem();  // the stage was read with plain loads
@@ -781,16 +933,22 @@ int chunks_per_lane(int K, int cap) {
     return std::min(cap, c <= 1 ? 1 : c <= 2 ? 2 : 4);
 }
 
-// Stages per warp that fit the ring budget less `other` bytes (0: the ring
-// path does not apply).
-int ring_stages(size_t stage_bytes, size_t other = 0) {
-    if (other >= (size_t)kRingSmemBudget) return 0;
-    const size_t per_warp = (kRingSmemBudget - other) / kGemvWarps;
+// Shared memory of the staged H rows and their chunk sums (down kernel, T == 1).
+size_t staged_h_bytes(int rows, int ldh) {
+    return (size_t)rows * ldh * 2 + (size_t)rows * (ldh / 32) * 4;
+}
+
+// Stages per warp that fit `budget` less `other` bytes over `warps` rings (0:
+// the ring path does not apply).
+int ring_stages(size_t stage_bytes, size_t budget, int warps, size_t other = 0) {
+    if (other >= budget) return 0;
+    const size_t per_warp = (budget - other) / warps;
     return (int)std::min<size_t>(kMaxRing, per_warp / stage_bytes);
 }
 
 template <typename Kern, typename... Args>
-cudaError_t launch_persistent(Kern kern, size_t smem, bool pdl, cudaStream_t st, Args... args) {
+cudaError_t launch_persistent(Kern kern, int threads, size_t smem, bool pdl, cudaStream_t st,
+                              Args... args) {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     if (smem) {
@@ -799,7 +957,7 @@ cudaError_t launch_persistent(Kern kern, size_t smem, bool pdl, cudaStream_t st,
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
-    cfg.blockDim = dim3(kGemvThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -813,24 +971,26 @@ cudaError_t launch_persistent(Kern kern, size_t smem, bool pdl, cudaStream_t st,
 template <int CPL>
 cudaError_t launch_gu(const GuArgs& a, bool one, int S, size_t stage, bool pdl, cudaStream_t st) {
     if (S >= 2) {
-        const size_t smem = (size_t)kGemvWarps * S * stage;
-        return one ? launch_persistent(gateup_ring_kernel<CPL, true>, smem, pdl, st, a, S)
-                   : launch_persistent(gateup_ring_kernel<CPL, false>, smem, pdl, st, a, S);
+        const size_t smem = (size_t)kGuWarps * S * stage;
+        return one ? launch_persistent(gateup_ring_kernel<CPL, true>, kGuThreads, smem, pdl, st, a, S)
+                   : launch_persistent(gateup_ring_kernel<CPL, false>, kGuThreads, smem, pdl, st, a, S);
     }
-    return one ? launch_persistent(gateup_gemv_kernel<CPL, true>, 0, pdl, st, a)
-               : launch_persistent(gateup_gemv_kernel<CPL, false>, 0, pdl, st, a);
+    return one ? launch_persistent(gateup_gemv_kernel<CPL, true>, kGuThreads, 0, pdl, st, a)
+               : launch_persistent(gateup_gemv_kernel<CPL, false>, kGuThreads, 0, pdl, st, a);
 }
 
 template <int CPL>
 cudaError_t launch_dn(const DnArgs& a, bool one, int S, size_t stage, int h_rows, bool pdl,
                       cudaStream_t st) {
     if (S >= 2) {
-        const size_t smem = (size_t)h_rows * a.ldh * 2 + (size_t)kGemvWarps * S * stage;
-        return one ? launch_persistent(down_ring_kernel<CPL, true>, smem, pdl, st, a, S, h_rows)
-                   : launch_persistent(down_ring_kernel<CPL, false>, smem, pdl, st, a, S, h_rows);
+        const size_t smem = staged_h_bytes(h_rows, a.ldh) + (size_t)kDnWarps * S * stage;
+        return one ? launch_persistent(down_ring_kernel<CPL, true>, kDnThreads, smem, pdl, st, a, S,
+                                       h_rows)
+                   : launch_persistent(down_ring_kernel<CPL, false>, kDnThreads, smem, pdl, st, a, S,
+                                       h_rows);
     }
-    return one ? launch_persistent(down_gemv_kernel<CPL, true>, 0, pdl, st, a)
-               : launch_persistent(down_gemv_kernel<CPL, false>, 0, pdl, st, a);
+    return one ? launch_persistent(down_gemv_kernel<CPL, true>, kDnThreads, 0, pdl, st, a)
+               : launch_persistent(down_gemv_kernel<CPL, false>, kDnThreads, 0, pdl, st, a);
 }
 
 bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
@@ -867,9 +1027,9 @@ cudaError_t launch_gateup_gemv(const uint16_t* x, const moe_dims_t& d, const int
     const bool one = d.T == 1 && single_pass;
     // ring: one stage holds a whole row pair, scale rows are 16-byte multiples
     const int scb = d.d / d.group * 2;
-    const size_t stage = (size_t)d.d + 2 * scb;
+    const size_t stage = (size_t)kGuRP * (d.d + 2 * scb);
     const bool ring_ok = single_pass && scb % 16 == 0 && aligned16(Wgu.s) && aligned16(Wgu_s.s);
-    const int S = ring_ok ? ring_stages(stage) : 0;
+    const int S = ring_ok ? ring_stages(stage, kGuRingBudget, kGuWarps) : 0;
     switch (cpl) {
         case 1: return launch_gu<1>(a, one, S, stage, pdl, st);
         case 2: return launch_gu<2>(a, one, S, stage, pdl, st);
@@ -913,9 +1073,8 @@ cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32
     const bool ring_ok = single_pass && sb_F % 16 == 0 && sb_Fs % 16 == 0 && aligned16(Wd.s) &&
                          aligned16(Wd_s.s);
     // a single token's H rows (k routed + 1 shared) are staged in shared memory
-    const size_t h_bytes = (size_t)(d.k + 1) * a.ldh * 2;
-    const int h_rows = (one && h_bytes <= kMaxStagedH) ? d.k + 1 : 0;
-    const int S = ring_ok ? ring_stages(stage, (size_t)h_rows * a.ldh * 2) : 0;
+    const int h_rows = (one && staged_h_bytes(d.k + 1, a.ldh) <= kMaxStagedH) ? d.k + 1 : 0;
+    const int S = ring_ok ? ring_stages(stage, kDnRingBudget, kDnWarps, staged_h_bytes(h_rows, a.ldh)) : 0;
     return cpl == 1 ? launch_dn<1>(a, one, S, stage, h_rows, pdl, st)
                     : launch_dn<2>(a, one, S, stage, h_rows, pdl, st);
 }
