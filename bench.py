@@ -112,7 +112,7 @@ class ClockSampler:
 
 def kernels_per_step(cfg, flags=0):
     """Kernels libmoe.so launches for one moe_layer_forward (memset nodes excluded)."""
-    gemv = (flags & 0x1) or (cfg.T <= 64 and not flags & 0x2)
+    gemv = (flags & 0x1) or (cfg.T <= 4 and not flags & 0x2)
     if gemv and cfg.T <= 64:
         return 3  # fused router + descriptors, gate+up GEMV, down GEMV + combine
     if gemv:
@@ -121,7 +121,7 @@ def kernels_per_step(cfg, flags=0):
 
 
 class GpuBench:
-    def __init__(self, cfg, device, ncopy: int, nbatch: int):
+    def __init__(self, cfg, device, ncopy: int, nbatch: int, flags: int = 0):
         import torch
 
         import moe_expert_layer_sigmoid_gb300 as moe
@@ -143,6 +143,7 @@ class GpuBench:
             self.copies.append((moe.w4(ts[0], ts[1]), moe.w4(ts[2], ts[3]), moe.w4(ts[4], ts[5]),
                                 moe.w4(ts[6], ts[7])))
         self.dims = L.dims()
+        self.dims.flags = flags
         self.ws = moe.workspace(moe.moe_layer_workspace_bytes(self.dims), device)
         self.out = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=device)
         self.stream = torch.cuda.Stream(device)
@@ -341,9 +342,9 @@ def gpu_roofline_prefill(cfg, gu_ms, pk, pk_kind):
             "peak_source": f"{pk_kind} bf16_tflops"}
 
 
-def measure_config(name, device, warmup, steps, ncopy, nbatch, pk, pk_kind, gpu_index):
+def measure_config(name, device, warmup, steps, ncopy, nbatch, pk, pk_kind, gpu_index, flags=0):
     cfg = workloads.CONFIGS[name]
-    b = GpuBench(cfg, device, ncopy=ncopy, nbatch=nbatch)
+    b = GpuBench(cfg, device, ncopy=ncopy, nbatch=nbatch, flags=flags)
     b.capture()
     clocks = ClockSampler(gpu_index)
     clocks.start()
@@ -445,6 +446,8 @@ def main():
     ap.add_argument("--ncopy", type=int, default=8)
     ap.add_argument("--nbatch", type=int, default=8)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--flags", type=int, default=0,
+                    help="moe_dims_t.flags for the headline config (1: force GEMV, 2: force grouped)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -465,7 +468,7 @@ def main():
     if world > 1:
         dist.barrier()
     main_res = measure_config(args.config, device, args.warmup, args.steps, args.ncopy,
-                              args.nbatch, pk, pk_kind, gpu_index)
+                              args.nbatch, pk, pk_kind, gpu_index, flags=args.flags)
     sec_res = None
     if args.secondary and args.secondary != args.config:
         sec_res = measure_config(args.secondary, device, args.warmup, args.secondary_steps,
@@ -508,8 +511,8 @@ def main():
                     "h2d_bytes_per_step": main_res["h2d"], "d2h_bytes_per_step": main_res["d2h"],
                     "ms_per_step": round(main_res["e2e_ms"], 5),
                     "mode": "graph replay of moe_layer_forward_host (pinned host x and out)"},
-            "gpu_launches": kernels_per_step(cfg) * args.steps,
-            "kernels_per_step": kernels_per_step(cfg),
+            "gpu_launches": kernels_per_step(cfg, args.flags) * args.steps,
+            "kernels_per_step": kernels_per_step(cfg, args.flags),
             "cpu_baseline": cpu,
             "peaks": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback",
         }

@@ -87,7 +87,8 @@ typedef struct {
 #define MOE_FLAG_FORCE_GROUPED 0x2u /* run the experts on the tcgen05 grouped path    */
 #define MOE_FLAG_NO_SCHED 0x4u      /* grouped path: expert-id order, no N-banding     */
 
-/* Packed int4 weights: q [rows][K/2] bytes, s [rows][K/group] fp16 (device). */
+/* Packed int4 weights: q [rows][K/2] bytes, s [rows][K/group] fp16 (device);
+   q 16-byte aligned, s 2-byte aligned (MOE_ERR_INVALID_ARG otherwise). */
 typedef struct {
     const uint8_t* q;
     const uint16_t* s;
@@ -202,8 +203,11 @@ moe_status_t moe_build_descriptors(const int32_t* topk_idx, const moe_dims_t* di
  *   Wgu_s    shared gate+up, q [2F_s][d/2], s [2F_s][d/group]
  *   H        (device) out: bf16 [T*k + T][max(F, F_s)] (row stride max(F, F_s))
  *   ws       the workspace moe_build_descriptors filled for this batch
- * T <= 64 runs a CUDA-core GEMV, larger T the tcgen05 grouped kernel (the
- * flags can force either).
+ * T <= 4 runs a CUDA-core GEMV, larger T the tcgen05 grouped kernel; the
+ * flags can force either (the GEMV needs d <= 4096 and max(F, F_s) <= 2048,
+ * the grouped kernel d, F, F_s multiples of 128 and at most 32 quantisation
+ * groups per row; a forced path that does not cover the shape returns
+ * MOE_ERR_UNSUPPORTED).
  */
 moe_status_t moe_gateup_swiglu_w4a16(const uint16_t* x, const moe_dims_t* dims,
                                      const int32_t* offsets, const int32_t* perm,
@@ -240,7 +244,13 @@ moe_status_t moe_combine_shared(const float* Y, const float* topk_w, const int32
 /* ----------------------------------------------------------------------------
  * moe_layer_forward -- the whole layer in one call: router, descriptors,
  * gate+up SwiGLU, down, combine, with the intermediates in the workspace.
- * Same arguments as the calls above; ws must hold moe_layer_workspace_bytes.
+ * Same arguments as the calls above; ws must hold moe_layer_workspace_bytes
+ * and be zero-filled before its first use (the single-launch decode router
+ * keeps a completion counter in it, which every call leaves at zero).
+ * On the GEMV path (T <= 4 by default) the call is three launches chained by
+ * programmatic dependent launch: the router with the top-k and descriptors in
+ * its last CTA, gate+up, and down with the combine fused in; otherwise the
+ * router, descriptors, grouped gate+up and down, and combine.
  * Graph-capturable.
  */
 size_t moe_layer_workspace_bytes(const moe_dims_t* dims);

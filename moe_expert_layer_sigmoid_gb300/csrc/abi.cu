@@ -138,15 +138,16 @@ T* ws_at(void* ws, size_t off) {
 }
 
 // Expert path: CUDA-core GEMV for small T (or when forced), the tcgen05
-// grouped kernel otherwise.  Shapes the grouped kernel does not cover run on
-// the GEMV unless the grouped path is forced, which then reports UNSUPPORTED.
+// grouped kernel otherwise.  A shape only one of them covers runs there; a
+// forced path that does not cover the shape reports UNSUPPORTED.
 enum class Path { kGemv, kGrouped, kUnsupported };
 
 Path expert_path(const moe_dims_t& d) {
-    if (d.flags & MOE_FLAG_FORCE_GEMV) return Path::kGemv;
-    const bool ok = grouped_supported(d);
-    if (d.flags & MOE_FLAG_FORCE_GROUPED) return ok ? Path::kGrouped : Path::kUnsupported;
-    return (d.T > kGemvMaxT && ok) ? Path::kGrouped : Path::kGemv;
+    const bool gemv = gemv_supported(d), grouped = grouped_supported(d);
+    if (d.flags & MOE_FLAG_FORCE_GEMV) return gemv ? Path::kGemv : Path::kUnsupported;
+    if (d.flags & MOE_FLAG_FORCE_GROUPED) return grouped ? Path::kGrouped : Path::kUnsupported;
+    if (grouped && (d.T > kGemvMaxT || !gemv)) return Path::kGrouped;
+    return gemv ? Path::kGemv : Path::kUnsupported;
 }
 
 moe_status_t gateup_impl(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,

@@ -59,8 +59,14 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 constexpr int kRouterSmallT = 64;
 constexpr int kRouterKChunk = 1024;
 
-// GEMV (decode) expert path for T <= kGemvMaxT unless forced.
-constexpr int kGemvMaxT = 64;
+// GEMV (decode) expert path by default for T <= kGemvMaxT (the CUDA-core GEMV
+// redoes its dequantisation per 4-token pass and is FMA-bound beyond a few
+// tokens: at T = 32 the grouped tensor-core kernel measured 6x faster); the
+// flags can force it for any T <= kMaxDecodeT.  One pass of its loads covers
+// rows of up to kGemvMaxD (gate+up) / kGemvMaxF (down) elements.
+constexpr int kGemvMaxT = 4;
+constexpr int kGemvMaxD = 4096;
+constexpr int kGemvMaxF = 2048;
 
 // Fused decode router (decode.cu) limits.
 constexpr int kMaxDecodeT = 64;
@@ -92,6 +98,7 @@ cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int
 // launches with programmatic stream serialisation: the kernel's prologue
 // overlaps the previous kernel, and it waits for it before reading its
 // outputs.  With `out` non-null the down kernel also does the combine.
+bool gemv_supported(const moe_dims_t& d);
 cudaError_t launch_gateup_gemv(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,
                                const int32_t* perm, const int32_t* sched, moe_w4_t Wgu,
                                moe_w4_t Wgu_s, uint16_t* H, const int32_t* n_active,
