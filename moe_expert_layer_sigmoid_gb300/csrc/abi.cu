@@ -16,7 +16,8 @@ WsLayout ws_layout(const moe_dims_t& d) {
     const int64_t rows = slots + T;
     const int64_t Fmax = std::max(d.F, d.F_s);
     L.router_ksplit = (d.d % 512 == 0) ? d.d / 512 : d.d / 256;
-    const int64_t ks = T <= kRouterSmallT ? L.router_ksplit : 1;
+    L.router_ksplit_large = router_ksplit_large(d);
+    const int64_t ks = T <= kRouterSmallT ? L.router_ksplit : L.router_ksplit_large;
     // tile lists: one entry per (group, 128-row weight band, 128-token tile)
     const int64_t groups = std::min<int64_t>(E, slots) + 1;
     const int64_t tok_tiles = (slots + kTileN - 1) / kTileN + groups + (T + kTileN - 1) / kTileN;
@@ -233,7 +234,7 @@ moe_status_t moe_router_topk(const uint16_t* x, const float* W_r, const float* b
     if (!x || !W_r || !bias || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
     return map_err(launch_router(x, W_r, bias, *dims, topk_idx, topk_w, margin,
                                  ws_at<float>(ws, L.logits), L.router_ksplit,
-                                 static_cast<cudaStream_t>(stream)));
+                                 L.router_ksplit_large, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_build_descriptors(const int32_t* topk_idx, const moe_dims_t* dims,
@@ -323,7 +324,7 @@ moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float*
             if (e != cudaSuccess) return MOE_ERR_CUDA;
         } else {
             e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
-                              ws_at<float>(ws, L.logits), L.router_ksplit, s);
+                              ws_at<float>(ws, L.logits), L.router_ksplit, L.router_ksplit_large, s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
             e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
                                    ws_at<int4>(ws, L.tiles), L.max_tiles, s);
@@ -336,7 +337,7 @@ moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float*
                                         pos, out, hdr, true, s));
     }
     e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr, ws_at<float>(ws, L.logits),
-                      L.router_ksplit, s);
+                      L.router_ksplit, L.router_ksplit_large, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
                            ws_at<int4>(ws, L.tiles), L.max_tiles, s);

@@ -50,6 +50,7 @@ struct WsLayout {
     size_t topk_idx, topk_w, counts, offsets, perm, pos, sched, H, Y, x_stage, out_stage;
     size_t layer_bytes;
     int router_ksplit;    // K split of the small-T router
+    int router_ksplit_large;  // K split of the large-T router
     int64_t max_tiles;    // capacity of each tile list
 };
 
@@ -84,9 +85,12 @@ WsLayout ws_layout(const moe_dims_t& d);
 cudaError_t launch_pack_w4(const float* w, int64_t rows, int64_t K, int group, uint8_t* q,
                            uint16_t* s, cudaStream_t st);
 
+// Router: logits as split-K partials (ksplit slices for T <= kRouterSmallT,
+// ksplit_large above it), then the top-k.
+int router_ksplit_large(const moe_dims_t& d);
 cudaError_t launch_router(const uint16_t* x, const float* W_r, const float* bias,
                           const moe_dims_t& d, int32_t* topk_idx, float* topk_w, float* margin,
-                          float* logits, int ksplit, cudaStream_t st);
+                          float* logits, int ksplit, int ksplit_large, cudaStream_t st);
 
 cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int32_t* counts,
                                int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,

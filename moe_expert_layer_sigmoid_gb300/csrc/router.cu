@@ -29,57 +29,89 @@ __global__ void __launch_bounds__(256) router_logits_gemv(const uint16_t* __rest
 }
 
 // ---------------------------------------------------------------------------
-// Large T (prefill): 64 x 64 register-tiled SGEMM, logits[t][e] = x[t] . W_r[e].
-constexpr int kBM = 64, kBN = 64, kBK = 16;
+// Large T (prefill): register-blocked SGEMM, logits partial [kz][t][e] =
+// sum over the kz-th K slice of x[t][k] * W_r[e][k], fp32 products and sums.
+// CTA tile 128 tokens x 128 experts, 256 threads with 8 x 8 outputs each
+// (rows ty*4 + {0..3, 64..67}, columns tx*4 + {0..3, 64..67}), K step 8,
+// double-buffered shared memory filled from registers loaded one step ahead.
+// The K dimension is split over gridDim.z slices so that the grid covers the
+// GPU; the top-k sums the slices in order.
+constexpr int kSgBM = 128, kSgBN = 128, kSgBK = 8;
 
 __global__ void __launch_bounds__(256) router_logits_sgemm(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ W_r, int T,
-                                                          int d, int E, float* __restrict__ out) {
-    __shared__ float As[kBK][kBM + 4];
-    __shared__ float Bs[kBK][kBN + 4];
+                                                          int d, int E, int kchunk,
+                                                          float* __restrict__ partial) {
+    __shared__ __align__(16) float As[2][kSgBK][kSgBM];
+    __shared__ __align__(16) float Bs[2][kSgBK][kSgBN];
     const int tid = threadIdx.x;
-    const int t0 = blockIdx.y * kBM, e0 = blockIdx.x * kBN;
-    const int tx = tid & 15, ty = tid >> 4;  // 16 x 16 threads, 4 x 4 outputs each
-    float acc[4][4] = {};
-    // loader mapping: 64 rows x 16 k = 1024 elements = 256 threads x 4
-    const int lr = tid >> 2, lk = (tid & 3) * 4;
-    for (int kb = 0; kb < d; kb += kBK) {
-        {
-            const int t = t0 + lr;
-            float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
-            if (t < T) {
-                uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (int64_t)t * d + kb + lk));
-                v0 = bf16_lo(xv.x); v1 = bf16_hi(xv.x); v2 = bf16_lo(xv.y); v3 = bf16_hi(xv.y);
-            }
-            As[lk + 0][lr] = v0; As[lk + 1][lr] = v1; As[lk + 2][lr] = v2; As[lk + 3][lr] = v3;
-            const int e = e0 + lr;
-            float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < E) wv = __ldg(reinterpret_cast<const float4*>(W_r + (int64_t)e * d + kb + lk));
-            Bs[lk + 0][lr] = wv.x; Bs[lk + 1][lr] = wv.y; Bs[lk + 2][lr] = wv.z; Bs[lk + 3][lr] = wv.w;
+    const int e0 = blockIdx.x * kSgBN, t0 = blockIdx.y * kSgBM;
+    const int kz = blockIdx.z, kbeg = kz * kchunk;
+    const int tx = tid & 15, ty = tid >> 4;
+    // loader: row lr (token / expert) of the tile, 4 consecutive k at lk
+    const int lr = tid >> 1, lk = (tid & 1) * 4;
+    const int lt = t0 + lr, le = e0 + lr;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    auto load = [&](int k, uint2& xa, float4& wb) {
+        xa = lt < T ? __ldg(reinterpret_cast<const uint2*>(x + (int64_t)lt * d + k + lk)) : make_uint2(0, 0);
+        wb = le < E ? __ldg(reinterpret_cast<const float4*>(W_r + (int64_t)le * d + k + lk))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto store = [&](int buf, uint2 xa, float4 wb) {
+        As[buf][lk + 0][lr] = bf16_lo(xa.x);
+        As[buf][lk + 1][lr] = bf16_hi(xa.x);
+        As[buf][lk + 2][lr] = bf16_lo(xa.y);
+        As[buf][lk + 3][lr] = bf16_hi(xa.y);
+        Bs[buf][lk + 0][lr] = wb.x;
+        Bs[buf][lk + 1][lr] = wb.y;
+        Bs[buf][lk + 2][lr] = wb.z;
+        Bs[buf][lk + 3][lr] = wb.w;
+    };
+    uint2 xa;
+    float4 wb;
+    load(kbeg, xa, wb);
+    store(0, xa, wb);
+    __syncthreads();
+    const int nsteps = kchunk / kSgBK;
+    for (int s = 0; s < nsteps; ++s) {
+        const int buf = s & 1;
+        if (s + 1 < nsteps) load(kbeg + (s + 1) * kSgBK, xa, wb);
+#pragma unroll
+        for (int kk = 0; kk < kSgBK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4 + 64]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4 + 64]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
-        __syncthreads();
-#pragma unroll
-        for (int kk = 0; kk < kBK; ++kk) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
+        if (s + 1 < nsteps) store(buf ^ 1, xa, wb);
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
+    for (int i = 0; i < 8; ++i) {
+        const int t = t0 + ty * 4 + (i & 3) + (i >> 2) * 64;
         if (t >= T) continue;
+        float* row = partial + ((int64_t)kz * T + t) * E;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
-            if (e < E) out[(int64_t)t * E + e] = acc[i][j];
+        for (int jh = 0; jh < 2; ++jh) {
+            const int e = e0 + tx * 4 + jh * 64;
+            if (e + 3 < E) {
+                *reinterpret_cast<float4*>(row + e) =
+                    make_float4(acc[i][4 * jh], acc[i][4 * jh + 1], acc[i][4 * jh + 2], acc[i][4 * jh + 3]);
+            } else {
+                for (int j = 0; j < 4; ++j)
+                    if (e + j < E) row[e + j] = acc[i][4 * jh + j];
+            }
         }
     }
 }
@@ -101,9 +133,16 @@ __global__ void __launch_bounds__(256) router_topk(const float* __restrict__ par
 
 }  // namespace
 
+int router_ksplit_large(const moe_dims_t& d) {
+    const int64_t tiles = (int64_t)((d.T + kSgBM - 1) / kSgBM) * ((d.E + kSgBN - 1) / kSgBN);
+    int ks = 1;
+    while (ks * 2 <= d.d / 256 && tiles * ks * 2 <= 320) ks *= 2;
+    return ks;
+}
+
 cudaError_t launch_router(const uint16_t* x, const float* W_r, const float* bias,
                           const moe_dims_t& dm, int32_t* topk_idx, float* topk_w, float* margin,
-                          float* logits, int ksplit, cudaStream_t st) {
+                          float* logits, int ksplit, int ksplit_large, cudaStream_t st) {
     const int T = dm.T, d = dm.d, E = dm.E, k = dm.k;
     int ks = 1;
     if (T <= kRouterSmallT) {
@@ -111,8 +150,9 @@ cudaError_t launch_router(const uint16_t* x, const float* W_r, const float* bias
         dim3 grid((E + 7) / 8, ks);
         router_logits_gemv<<<grid, 256, 0, st>>>(x, W_r, T, d, E, d / ks, logits);
     } else {
-        dim3 grid((E + kBN - 1) / kBN, (T + kBM - 1) / kBM);
-        router_logits_sgemm<<<grid, 256, 0, st>>>(x, W_r, T, d, E, logits);
+        ks = ksplit_large;  // a power of two dividing d / 256
+        dim3 grid((E + kSgBN - 1) / kSgBN, (T + kSgBM - 1) / kSgBM, ks);
+        router_logits_sgemm<<<grid, 256, 0, st>>>(x, W_r, T, d, E, d / ks, logits);
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
