@@ -311,6 +311,12 @@ class GpuBench:
         self.torch.cuda.empty_cache()
 
 
+# DRAM bytes (read + write) per step of the decode chain at decode1, summed over
+# router_decode_kernel, gateup_gemv_kernel and down_gemv_kernel from one
+# `ncu --set full` capture of each on this code (cold caches).
+DECODE1_TRAFFIC = 4_269_312 + 48_120_832 + 30_976 + 23_850_240
+
+
 def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms):
     """The decode step against HBM.  Algorithmic bytes = packed int4 weights + fp16 scales
     of the active routed experts and of the shared expert (gate+up and down), per step.
@@ -323,7 +329,9 @@ def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms):
     router_bytes = cfg.E * cfg.d * 4
     return {"kernel": "decode step: router_decode_kernel + gateup_gemv_kernel + down_gemv_kernel",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None, "bytes_per_step": int(nbytes),
+            "frac": round(achieved / peak, 4),
+            "traffic": DECODE1_TRAFFIC if cfg.name == "decode1" else None,
+            "bytes_per_step": int(nbytes),
             "router_weight_bytes_not_counted": router_bytes,
             "step_us": round(ms * 1e3, 3),
             "standalone_gateup_us": round(gu_ms * 1e3, 3),
