@@ -20,17 +20,27 @@
 // once into that same row order (gather_rows_kernel), which replaces per-row
 // gathers inside the GEMM that the TMA unit serves slowly.
 //
-// Warp roles (16 warps, one CTA per SM):
+// Warp roles (20 warps, one CTA per SM; setmaxnreg moves registers from the
+// control warpgroup to the epilogue's):
 //   warp 0      TMA producer: per tile the fp16 scale block (bulk copy), per
 //               stage the int4 weight tile (64B swizzle) and the activation
 //               tile (128B swizzle, the UMMA K-major canonical layout)
-//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16, A from
-//               TMEM, B from shared memory, fp32 accumulator in TMEM
-//   warps 2-3   idle
-//   warps 4-7   dequantisers: int4 -> bf16 integers (exact), tcgen05.st to TMEM
-//   warps 8-15  epilogue: per quantisation group, read the group's partial
-//               sums from TMEM and accumulate s * partial in fp32 registers;
-//               at the end of a tile apply SwiGLU (gate+up) or store Y (down)
+//   warps 1-2   MMA issuers (warp 1 also allocates TMEM): tcgen05.mma
+//               kind::f16, A from TMEM, B from shared memory, fp32 accumulator
+//               in TMEM; even quantisation groups on warp 1, odd on warp 2
+//   warp 3      idle
+//   warps 4-11  dequantisers, two per TMEM lane quarter (warps 4-7 the first
+//               64 K of a stage, 8-11 the second): int4 -> bf16 integers
+//               (exact), tcgen05.st to TMEM
+//   warps 12-19 epilogue, two per lane quarter (warps 12-15 columns 0-63,
+//               16-19 columns 64-127): per quantisation group, read the
+//               group's partial sums from TMEM and accumulate s * partial in
+//               fp32 registers (packed f32x2 FMAs); at the end of a tile apply
+//               SwiGLU (gate+up) or store Y (down)
+//
+// One dequantiser warp per quarter was the bound (a stage's 128 x 128 int4
+// tile took it ~900 cycles, latency-bound, against ~550 for the stage's
+// MMAs); two halve its share.
 //
 // Numerics: each group's partial sum is sum_k x_k * q_k with exact bf16
 // products and fp32 accumulation; multiplying by the fp16 scale s in fp32
@@ -47,10 +57,19 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 20;
 constexpr int kThreads = kWarps * 32;
 constexpr int kDequantWarp0 = 4;
-constexpr int kEpilogueWarp0 = 8;
+constexpr int kDequantWarps = 8;
+constexpr int kEpilogueWarp0 = 12;
+constexpr int kEpilogueWarps = 8;
+// Registers per thread after setmaxnreg: control warpgroup (warps 0-3),
+// dequantisers (4-11), epilogue (12-19).  Their sum over the CTA must not
+// exceed what the launch holds (checked on the host before every launch:
+// a setmaxnreg.inc that cannot be served would wait forever).
+constexpr int kRegCtl = 32, kRegDq = 72, kRegEpi = 152;
+constexpr int kRegBudget = 128 * (kRegCtl + 2 * kRegDq + 2 * kRegEpi);
+static_assert(kRegBudget <= 65536, "register split exceeds the register file");
 constexpr int kStages = 5;                        // shared-memory pipeline depth
 constexpr int kAStagesT = 4;                      // A operand stages in TMEM
 constexpr int kDBufs = 2;                         // accumulator buffers in TMEM
@@ -217,6 +236,14 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* v) {
         : "memory");
 }
 
+// a0 += s * v0, a1 += s * v1 as one packed f32x2 FMA (each lane rounds as fmaf)
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float v0, float v1) {
+    asm("{\n .reg .b64 acc, vv, ss;\n mov.b64 acc, {%0, %1};\n mov.b64 vv, {%2, %3};\n"
+        " mov.b64 ss, {%4, %4};\n fma.rn.f32x2 acc, ss, vv, acc;\n mov.b64 {%0, %1}, acc;\n}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(v0), "f"(v1), "f"(s));
+}
+
 // ---------------------------------------------------------------- tiles
 struct TileInfo {
     int grp;    // expert id, -1 for the shared expert
@@ -274,16 +301,18 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarFull + s), 1);
-            mbar_init(bar(kBarEmpty + s), 1 + 4);  // MMA commit + 4 dequant warps
+            // the MMA commit(s) of the stage (both issuers when it holds two or more
+            // groups) + the dequant warps
+            mbar_init(bar(kBarEmpty + s), (kKStage / G >= 2 ? 2 : 1) + kDequantWarps);
         }
-        for (int a = 0; a < kAStagesT; ++a) mbar_init(bar(kBarAReady + a), 4);
+        for (int a = 0; a < kAStagesT; ++a) mbar_init(bar(kBarAReady + a), kDequantWarps);
         for (int b = 0; b < kDBufs; ++b) {
             mbar_init(bar(kBarDFull + b), 1);
-            mbar_init(bar(kBarDEmpty + b), 8);
+            mbar_init(bar(kBarDEmpty + b), kEpilogueWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kBarScFull + b), 1);
-            mbar_init(bar(kBarScEmpty + b), 8);
+            mbar_init(bar(kBarScEmpty + b), kEpilogueWarps);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -307,7 +336,10 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
     const int n_tiles = *reinterpret_cast<volatile int*>(&p.hdr->n_tiles[p.mode]);
     const int grid = gridDim.x;
 
-    if (warp == 0) {
+    if (warp < kDequantWarp0) {
+      // each warpgroup changes its register count inside its own branch
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
+      if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t it = 0;
@@ -363,10 +395,16 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     mbar_wait(bar(kBarFull + j % kStages), (j / kStages) & 1, abort_flag, p.hdr);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+      } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two issuers on two schedulers: group gi (its own accumulator buffer
+        // gi & 1, fresh at its first K step) is issued by warp 1 + (gi & 1).
+        // One issuing thread spent most of each stage on barrier and commit
+        // latency next to the dequantiser and epilogue warps of its scheduler.
+        const uint32_t me = (uint32_t)(warp - 1);
         if (lane == 0) {
             uint32_t it = 0, gi = 0;
+            int64_t last = -1;  // last stage this issuer committed
             bool ok = true;
             int4 cur = load_tile(p, blockIdx.x, n_tiles);
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
@@ -376,19 +414,26 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 const int nks = ti.K / kKStage;
                 for (int ks = 0; ks < nks && ok; ++ks, ++it) {
                     const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
                     const int ta = it % kAStagesT;
                     const uint32_t tph = (it / kAStagesT) & 1;
-                    if (!mbar_wait(bar(kBarFull + s), ph, abort_flag, p.hdr) ||
-                        !mbar_wait(bar(kBarAReady + ta), tph, abort_flag, p.hdr)) { ok = false; break; }
+                    constexpr int kGroups = kKStage / G;
+                    if (kGroups == 1 && (gi & 1) != me) {  // the other issuer's stage
+                        ++gi;
+                        continue;
+                    }
+                    // AREADY completes only after every dequantiser warp has seen FULL for
+                    // this stage (A and B land on the same barrier), so it also orders the
+                    // B tile before the MMAs
+                    if (!mbar_wait(bar(kBarAReady + ta), tph, abort_flag, p.hdr)) { ok = false; break; }
                     tc_fence_after();
                     // descriptor of the stage's B tile; K steps add (kg/4)*16 KB + (kg%4)*32 B,
                     // i.e. (kg/4)*1024 + (kg%4)*2 in the 16-byte address field
                     const uint64_t bdesc0 = smem_desc_sw128(sbase + kOffB + s * kBStageBytes);
                     const uint32_t a0 = tmem + (uint32_t)(ta * 64);
 #pragma unroll
-                    for (int gg = 0; gg < kKStage / G; ++gg, ++gi) {
+                    for (int gg = 0; gg < kGroups; ++gg, ++gi) {
                         const int b = gi & 1;
+                        if ((uint32_t)b != me) continue;
                         if (!mbar_wait(bar(kBarDEmpty + b), ((gi >> 1) & 1) ^ 1, abort_flag, p.hdr)) {
                             ok = false;
                             break;
@@ -406,17 +451,21 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     }
                     if (!ok) break;
                     mma_commit(bar(kBarEmpty + s));
+                    last = it;
                 }
                 cur = nxt;
             }
-            // the last commit has landed before the CTA can exit
-            if (ok && it > 0)
-                mbar_wait(bar(kBarEmpty + (it - 1) % kStages), ((it - 1) / kStages) & 1, abort_flag, p.hdr);
+            // this issuer's last commit has landed before the CTA can exit
+            if (ok && last >= 0)
+                mbar_wait(bar(kBarEmpty + last % kStages), (uint32_t)(last / kStages) & 1, abort_flag, p.hdr);
         }
         __syncwarp();
-    } else if (warp >= kDequantWarp0 && warp < kEpilogueWarp0) {
+      }
+    } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------------ dequantisers
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegDq));
         const int q = warp & 3;
+        const int h = (warp - kDequantWarp0) >> 2;  // which 64 K of the stage
         const int m = q * 32 + lane;  // tile row = TMEM lane
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t it = 0;
@@ -430,16 +479,16 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
                 if (!mbar_wait(bar(kBarFull + s), ph, abort_flag, p.hdr)) { ok = false; break; }
-                // row m of the int4 tile: 64 bytes, 16-byte chunks 64B-swizzled by the TMA
+                // row m of the int4 tile: 64 bytes, 16-byte chunks 64B-swizzled by the TMA;
+                // this warp's half is chunks 2h and 2h + 1
                 const uint8_t* arow = smem + kOffA + s * kAStageBytes + m * 64;
-                uint4 v[4];
+                uint4 v[2];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    v[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ ((m >> 1) & 3)) << 4));
+                for (int c = 0; c < 2; ++c)
+                    v[c] = *reinterpret_cast<const uint4*>(arow + (((2 * h + c) ^ ((m >> 1) & 3)) << 4));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarEmpty + s));
-                // first half of the row (K 0..63), stored while the second half converts
-                uint32_t r[64];
+                uint32_t r[32];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     nib8_to_bf16x2(v[c].x, r + 16 * c + 0);
@@ -456,15 +505,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     }
                 }
                 tc_fence_after();
-                tmem_st_x32(tmem + lane_base + (uint32_t)(ta * 64), r);
-#pragma unroll
-                for (int c = 2; c < 4; ++c) {
-                    nib8_to_bf16x2(v[c].x, r + 16 * c + 0);
-                    nib8_to_bf16x2(v[c].y, r + 16 * c + 4);
-                    nib8_to_bf16x2(v[c].z, r + 16 * c + 8);
-                    nib8_to_bf16x2(v[c].w, r + 16 * c + 12);
-                }
-                tmem_st_x32(tmem + lane_base + (uint32_t)(ta * 64 + 32), r + 32);
+                tmem_st_x32(tmem + lane_base + (uint32_t)(ta * 64 + 32 * h), r);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
@@ -472,8 +513,9 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
             }
             cur = nxt;
         }
-    } else if (warp >= kEpilogueWarp0) {
+    } else {
         // ------------------------------------------------------------ epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegEpi));
         // After a failed wait every epilogue warp keeps walking the same tiles
         // (skipping the work), so no warp waits on a barrier the others left.
         const int q = warp & 3;
@@ -506,18 +548,20 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 const float s = __half2float(srow[g]);
                 const uint32_t dcol = tmem + lane_base + (uint32_t)(kTmemD + b * 128 + col0);
                 if (col0 < ti.npad) {
-                    uint32_t v[32];
+                    uint32_t v[64];
+                    const bool two = col0 + 32 < ti.npad;
                     tmem_ld_x32(dcol, v);
+                    if (two) tmem_ld_x32(dcol + 32, v + 32);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] = fmaf(s, __uint_as_float(v[j]), acc[j]);
-                }
-                if (col0 + 32 < ti.npad) {
-                    uint32_t v[32];
-                    tmem_ld_x32(dcol + 32, v);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    for (int j = 0; j < 32; j += 2)
+                        ffma2(acc[j], acc[j + 1], s, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+                    if (two) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[32 + j] = fmaf(s, __uint_as_float(v[j]), acc[32 + j]);
+                        for (int j = 32; j < 64; j += 2)
+                            ffma2(acc[j], acc[j + 1], s, __uint_as_float(v[j]),
+                                  __uint_as_float(v[j + 1]));
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -526,7 +570,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(bar(kBarScEmpty + sb));
             if (p.mode == kGateUp) {
-                // lane i holds gate row f, lane i ^ 16 the up row of the same f
+                // lane i holds gate row f, lane i ^ 16 the up row of the same f;
+                // the gate lanes store the first 32 of the warp's tokens, the up lanes the rest
                 uint16_t* H = reinterpret_cast<uint16_t*>(p.out);
                 const int f = 64 * ti.band + f_local;
                 const bool lo = (lane & 16) == 0;
@@ -537,8 +582,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     const float uv = lo ? other : acc[j];
                     const int nn = col0 + j;
                     if (ok && lo == (j < 32) && nn < ti.n) {
-                        const float h = gv / (1.0f + expf(-gv)) * uv;
-                        H[(int64_t)(ti.row0 + nn) * p.ld_out + f] = float_to_bf16_bits(h);
+                        const float hv = gv / (1.0f + expf(-gv)) * uv;
+                        H[(int64_t)(ti.row0 + nn) * p.ld_out + f] = float_to_bf16_bits(hv);
                     }
                 }
             } else if (ok) {
@@ -648,6 +693,15 @@ template <int G>
 cudaError_t launch_g(GroupedParams& prm, int sms, cudaStream_t st) {
     cudaError_t err = ensure_dynamic_smem((const void*)grouped_w4a16_kernel<G>, kSmemBytes);
     if (err != cudaSuccess) return err;
+    // the warpgroups' setmaxnreg targets must fit in the registers the launch holds
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa;
+        err = cudaFuncGetAttributes(&fa, grouped_w4a16_kernel<G>);
+        if (err != cudaSuccess) return err;
+        launch_regs = fa.numRegs;
+    }
+    if (launch_regs * kThreads < kRegBudget) return cudaErrorInvalidConfiguration;
     grouped_w4a16_kernel<G><<<sms, kThreads, kSmemBytes, st>>>(prm);
     return cudaGetLastError();
 }
