@@ -116,8 +116,8 @@ def kernels_per_step(cfg, flags=0):
     if gemv and cfg.T <= 64:
         return 3  # fused router + descriptors, gate+up GEMV, down GEMV + combine
     if gemv:
-        return 2 + 2 + 2  # router (2), descriptors (2), the two GEMVs (combine fused)
-    return 2 + 2 + 1 + 2 + 1  # router, descriptors, row gather, two grouped GEMMs, combine
+        return 2 + 4 + 2  # router (2), descriptors (4), the two GEMVs (combine fused)
+    return 2 + 4 + 1 + 2 + 1  # router, descriptors, row gather, two grouped GEMMs, combine
 
 
 class GpuBench:

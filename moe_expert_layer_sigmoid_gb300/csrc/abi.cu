@@ -33,6 +33,8 @@ WsLayout ws_layout(const moe_dims_t& d) {
     off += align256(sizeof(int4) * (size_t)(2 * L.max_tiles));
     L.xs = off;
     off += align256(sizeof(uint16_t) * (size_t)(rows * d.d));
+    L.hist = off;
+    off += align256(sizeof(int32_t) * (size_t)desc_blocks(slots) * (size_t)E);
     L.step_bytes = off;
 
     L.topk_idx = off;
@@ -248,7 +250,8 @@ moe_status_t moe_build_descriptors(const int32_t* topk_idx, const moe_dims_t* di
     if (!topk_idx || !counts || !offsets || !perm || !pos || !sched) return MOE_ERR_INVALID_ARG;
     return map_err(launch_descriptors(topk_idx, *dims, counts, offsets, perm, pos, sched,
                                       ws_at<WsHeader>(ws, L.header), ws_at<int4>(ws, L.tiles),
-                                      L.max_tiles, static_cast<cudaStream_t>(stream)));
+                                      L.max_tiles, ws_at<int32_t>(ws, L.hist),
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_gateup_swiglu_w4a16(const uint16_t* x, const moe_dims_t* dims,
@@ -327,7 +330,8 @@ moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float*
                               ws_at<float>(ws, L.logits), L.router_ksplit, L.router_ksplit_large, s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
             e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
-                                   ws_at<int4>(ws, L.tiles), L.max_tiles, s);
+                                   ws_at<int4>(ws, L.tiles), L.max_tiles,
+                                   ws_at<int32_t>(ws, L.hist), s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
         }
         e = launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, &hdr->n_active, hdr,
@@ -340,7 +344,7 @@ moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float*
                       L.router_ksplit, L.router_ksplit_large, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
-                           ws_at<int4>(ws, L.tiles), L.max_tiles, s);
+                           ws_at<int4>(ws, L.tiles), L.max_tiles, ws_at<int32_t>(ws, L.hist), s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if ((st = gateup_impl(x, d, offsets, perm, sched, Wgu, Wgu_s, H, ws, s)) != MOE_OK) return st;
     if ((st = down_impl(H, d, offsets, sched, Wd, Wd_s, Y, ws, s)) != MOE_OK) return st;

@@ -45,6 +45,7 @@ struct WsLayout {
     size_t logits;        // fp32 [ksplit][T][E] router logit partials
     size_t tiles;         // int4 tile descriptors of the grouped kernels
     size_t xs;            // bf16 [T*k + T][d] gathered activation rows (grouped path)
+    size_t hist;          // int32 [desc_blocks(T*k)][E] descriptor-sort histograms
     size_t step_bytes;
     // whole-layer workspace (moe_layer_workspace_bytes) adds the intermediates
     size_t topk_idx, topk_w, counts, offsets, perm, pos, sched, H, Y, x_stage, out_stage;
@@ -92,9 +93,12 @@ cudaError_t launch_router(const uint16_t* x, const float* W_r, const float* bias
                           const moe_dims_t& d, int32_t* topk_idx, float* topk_w, float* margin,
                           float* logits, int ksplit, int ksplit_large, cudaStream_t st);
 
+// `hist` is workspace of desc_blocks(T * k) * E int32 (per-block histograms).
+int desc_blocks(int64_t nslots);
 cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int32_t* counts,
                                int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,
-                               WsHeader* hdr, int4* tiles, int64_t max_tiles, cudaStream_t st);
+                               WsHeader* hdr, int4* tiles, int64_t max_tiles, int32_t* hist,
+                               cudaStream_t st);
 
 // Decode expert GEMVs (experts_gemv.cu).  `n_active` is the count of routed
 // groups with rows (the workspace header's, written by the fused router) or
@@ -157,6 +161,15 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 }
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// a0 += s * v0, a1 += s * v1 as one packed f32x2 FMA (sm_100 family); each
+// lane rounds exactly as fmaf, so results match the scalar form bit for bit.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float v0, float v1) {
+    asm("{\n .reg .b64 acc, vv, ss;\n mov.b64 acc, {%0, %1};\n mov.b64 vv, {%2, %3};\n"
+        " mov.b64 ss, {%4, %4};\n fma.rn.f32x2 acc, ss, vv, acc;\n mov.b64 {%0, %1}, acc;\n}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(v0), "f"(v1), "f"(s));
+}
 
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue / wait until the previous kernel has completed and its writes are

@@ -14,25 +14,98 @@
 //   pos[s]     row of slot s (inverse of perm)
 //   sched[i]   experts by count, largest first, ties to the lower id
 //
-// The sort is a stable counting sort: a count pass, then one CTA per expert
-// that computes its offset and its schedule rank from the counts and
-// compacts that expert's slots in slot order.  Nothing depends on the order in
-// which atomics land, so the result is bit-reproducible.
+// The sort is a stable counting sort over blocks of 1024 slots: per-block
+// expert histograms, their sums and per-block prefixes (one thread per
+// expert), one CTA per expert for its offset, schedule rank and tiles, and a
+// placement pass in which every block writes its slots at
+//   offsets[e] + (earlier blocks' slots of e) + (earlier slots of e in this block),
+// the last term from warp-range prefixes and a match within each 32-slot
+// chunk.  Nothing depends on the order in which atomics land, so the result
+// is bit-reproducible.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-__global__ void desc_count(const int32_t* __restrict__ topk_idx, int64_t nslots, int E,
-                           int32_t* __restrict__ counts, WsHeader* hdr) {
-    for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < nslots;
-         s += (int64_t)gridDim.x * blockDim.x) {
-        const int e = topk_idx[s];
+constexpr int kDescSlots = 1024;   // slots per block of the counting sort
+constexpr int kDescThreads = 256;  // 8 warps of 128 slots each
+
+// Per-block expert histogram: hist[b][e] = slots of block b routed to e.
+__global__ void __launch_bounds__(kDescThreads)
+desc_hist(const int32_t* __restrict__ topk_idx, int64_t nslots, int E, int32_t* __restrict__ hist,
+          WsHeader* hdr) {
+    extern __shared__ int h_smem[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) h_smem[e] = 0;
+    __syncthreads();
+    const int64_t s0 = (int64_t)blockIdx.x * kDescSlots;
+    for (int i = threadIdx.x; i < kDescSlots; i += blockDim.x) {
+        const int64_t s = s0 + i;
+        if (s >= nslots) break;
+        const int e = __ldg(topk_idx + s);
         if (e < 0 || e >= E) {
             record_error(hdr, kErrBadExpertId);
             continue;
         }
-        atomicAdd(counts + e, 1);
+        atomicAdd(h_smem + e, 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = h_smem[e];
+}
+
+// counts[e] = sum over blocks; hist[b][e] becomes the exclusive prefix over blocks.
+__global__ void desc_counts(int32_t* __restrict__ hist, int nblk, int E, int32_t* __restrict__ counts) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+        const int c = hist[(int64_t)b * E + e];
+        hist[(int64_t)b * E + e] = run;
+        run += c;
+    }
+    counts[e] = run;
+}
+
+// Stable placement of block b's slots: perm[row] = slot, pos[slot] = row.
+__global__ void __launch_bounds__(kDescThreads)
+desc_place(const int32_t* __restrict__ topk_idx, int64_t nslots, int E,
+           const int32_t* __restrict__ offsets, const int32_t* __restrict__ blkoff,
+           int32_t* __restrict__ perm, int32_t* __restrict__ pos) {
+    extern __shared__ int w_smem[];  // [8 warps][E]: slots of e in earlier warp ranges, then running
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kWarps = kDescThreads / 32, kRange = kDescSlots / kWarps;
+    const int64_t s0 = (int64_t)blockIdx.x * kDescSlots + warp * kRange;
+    for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) w_smem[i] = 0;
+    __syncthreads();
+    int* mine = w_smem + warp * E;
+    for (int c = 0; c < kRange; c += 32) {  // warp range histogram
+        const int64_t s = s0 + c + lane;
+        const int e = s < nslots ? __ldg(topk_idx + s) : -1;
+        if (e >= 0 && e < E) atomicAdd(mine + e, 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {  // exclusive prefix over the warps
+        int run = offsets[e] + blkoff[(int64_t)blockIdx.x * E + e];
+        for (int w = 0; w < kWarps; ++w) {
+            const int c = w_smem[w * E + e];
+            w_smem[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int c = 0; c < kRange; c += 32) {
+        const int64_t s = s0 + c + lane;
+        const int e = s < nslots ? __ldg(topk_idx + s) : -1;
+        const bool ok = e >= 0 && e < E;
+        const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
+        if (ok) {
+            const int r = mine[e] + __popc(grp & lt);
+            perm[r] = (int32_t)s;
+            pos[s] = r;
+        }
+        __syncwarp();
+        if (ok && (grp & lt) == 0) mine[e] += __popc(grp);  // the group's first lane
+        __syncwarp();
     }
 }
 
@@ -70,12 +143,9 @@ __device__ __forceinline__ void write_group_tiles(int4* tiles, int list, int64_t
 }
 
 __global__ void __launch_bounds__(kScatterThreads)
-desc_scatter(const int32_t* __restrict__ topk_idx, int64_t nslots, int E,
-             const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-             int32_t* __restrict__ perm, int32_t* __restrict__ pos, int32_t* __restrict__ sched,
-             WsHeader* hdr, int4* __restrict__ tiles, TileGeom tg) {
+desc_plan(int64_t nslots, int E, const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+          int32_t* __restrict__ sched, WsHeader* hdr, int4* __restrict__ tiles, TileGeom tg) {
     __shared__ int red[6][kScatterThreads / 32];
-    __shared__ int warp_tot[kScatterThreads / 32];
     const bool shared_cta = blockIdx.x == E;  // the last CTA schedules the shared expert
     const int e = shared_cta ? 0 : blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -156,46 +226,28 @@ desc_scatter(const int32_t* __restrict__ topk_idx, int64_t nslots, int E,
         write_group_tiles(tiles, 1, (int64_t)(ntt_sh + tb) * tg.nb_dn, e, base_row, my_count,
                           tg.nb_dn, tg.sched, tg.max_tiles, hdr);
     }
-    if (my_count == 0) return;
-    int running = 0;
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int64_t b = 0; b < nslots; b += kScatterThreads) {
-        const int64_t s = b + tid;
-        const bool hit = s < nslots && topk_idx[s] == e;
-        const unsigned ball = __ballot_sync(0xffffffffu, hit);
-        if (lane == 0) warp_tot[warp] = __popc(ball);
-        __syncthreads();
-        int before = running, blk = 0;
-        for (int w = 0; w < kScatterThreads / 32; ++w) {
-            if (w < warp) before += warp_tot[w];
-            blk += warp_tot[w];
-        }
-        if (hit) {
-            const int r = base_row + before + __popc(ball & lt_mask);
-            perm[r] = (int32_t)s;
-            pos[s] = r;
-        }
-        running += blk;
-        __syncthreads();
-        if (running >= my_count) break;
-    }
 }
 
 }  // namespace
 
+int desc_blocks(int64_t nslots) { return (int)((nslots + kDescSlots - 1) / kDescSlots); }
+
 cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int32_t* counts,
                                int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,
-                               WsHeader* hdr, int4* tiles, int64_t max_tiles, cudaStream_t st) {
+                               WsHeader* hdr, int4* tiles, int64_t max_tiles, int32_t* hist,
+                               cudaStream_t st) {
     const int64_t nslots = (int64_t)d.T * d.k;
-    cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)d.E, st);
+    const int nblk = desc_blocks(nslots);
+    const size_t hist_smem = sizeof(int) * (size_t)d.E;
+    const size_t place_smem = sizeof(int) * (size_t)(kDescThreads / 32) * d.E;
+    cudaError_t err = ensure_dynamic_smem((const void*)desc_place, place_smem);
     if (err != cudaSuccess) return err;
-    const int threads = 256;
-    int blocks = (int)((nslots + threads - 1) / threads);
-    if (blocks > 1024) blocks = 1024;
-    if (blocks < 1) blocks = 1;
-    desc_count<<<blocks, threads, 0, st>>>(topk_idx, nslots, d.E, counts, hdr);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    if (nblk > 0) {
+        desc_hist<<<nblk, kDescThreads, hist_smem, st>>>(topk_idx, nslots, d.E, hist, hdr);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    desc_counts<<<(d.E + 255) / 256, 256, 0, st>>>(hist, nblk, d.E, counts);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     TileGeom tg;
     tg.T = d.T;
     tg.k = d.k;
@@ -204,9 +256,14 @@ cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int
     tg.nb_dn = d.d / 128;
     tg.sched = !(d.flags & MOE_FLAG_NO_SCHED);
     tg.max_tiles = max_tiles;
-    desc_scatter<<<d.E + 1, kScatterThreads, 0, st>>>(topk_idx, nslots, d.E, counts, offsets,
-                                                      perm, pos, sched, hdr, tiles, tg);
-    return cudaGetLastError();
+    desc_plan<<<d.E + 1, kScatterThreads, 0, st>>>(nslots, d.E, counts, offsets, sched, hdr, tiles, tg);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (nblk > 0) {
+        desc_place<<<nblk, kDescThreads, place_smem, st>>>(topk_idx, nslots, d.E, offsets, hist,
+                                                            perm, pos);
+        err = cudaGetLastError();
+    }
+    return err;
 }
 
 }  // namespace moe

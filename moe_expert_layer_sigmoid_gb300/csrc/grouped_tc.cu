@@ -32,8 +32,8 @@
 //   warps 4-11  dequantisers, two per TMEM lane quarter (warps 4-7 the first
 //               64 K of a stage, 8-11 the second): int4 -> bf16 integers
 //               (exact), tcgen05.st to TMEM
-//   warps 12-19 epilogue, two per lane quarter (warps 12-15 columns 0-63,
-//               16-19 columns 64-127): per quantisation group, read the
+//   warps 12-19 epilogue, two per lane quarter (warps 12-15 columns 0-31 and
+//               64-95, 16-19 columns 32-63 and 96-127): per group, read the
 //               group's partial sums from TMEM and accumulate s * partial in
 //               fp32 registers (packed f32x2 FMAs); at the end of a tile apply
 //               SwiGLU (gate+up) or store Y (down)
@@ -46,7 +46,8 @@
 // products and fp32 accumulation; multiplying by the fp16 scale s in fp32
 // gives sum_k x_k * (q_k * s), the dequantised product, without rounding the
 // weights.  TMEM: two A stages at columns [0, 128), three 128-column
-// accumulators at [128, 512).
+// accumulators at [128, 512), so the MMAs can run two groups ahead of the
+// epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -71,8 +72,8 @@ constexpr int kRegCtl = 32, kRegDq = 72, kRegEpi = 152;
 constexpr int kRegBudget = 128 * (kRegCtl + 2 * kRegDq + 2 * kRegEpi);
 static_assert(kRegBudget <= 65536, "register split exceeds the register file");
 constexpr int kStages = 5;                        // shared-memory pipeline depth
-constexpr int kAStagesT = 4;                      // A operand stages in TMEM
-constexpr int kDBufs = 2;                         // accumulator buffers in TMEM
+constexpr int kAStagesT = 2;                      // A operand stages in TMEM
+constexpr int kDBufs = 3;                         // accumulator buffers in TMEM
 static_assert(kAStagesT < kStages, "dequant reuses the stage barrier of the MMA it waits for");
 constexpr int kKStage = 128;                      // K elements per stage
 constexpr int kTokTile = 128;                     // max tokens (N) per tile
@@ -88,7 +89,8 @@ constexpr int kOffB = 0;
 constexpr int kOffA = kOffB + kStages * kBStageBytes;
 constexpr int kOffSc = kOffA + kStages * kAStageBytes;
 constexpr int kOffBar = kOffSc + 2 * kScBytes;
-// barriers: FULL[kStages], EMPTY[kStages], AREADY[kAStagesT], DFULL[2], DEMPTY[2], SCFULL[2], SCEMPTY[2]
+// barriers: FULL[kStages], EMPTY[kStages], AREADY[kAStagesT], DFULL[kDBufs], DEMPTY[kDBufs],
+// SCFULL[2], SCEMPTY[2]
 // EMPTY[s] completes when the MMAs of smem stage s are done and the dequant
 // warps have read its int4 tile; it also tells the dequant warps that the
 // TMEM A stage those MMAs read is free again.
@@ -234,14 +236,6 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* v) {
           "=r"(v[31])
         : "r"(taddr)
         : "memory");
-}
-
-// a0 += s * v0, a1 += s * v1 as one packed f32x2 FMA (each lane rounds as fmaf)
-__device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float v0, float v1) {
-    asm("{\n .reg .b64 acc, vv, ss;\n mov.b64 acc, {%0, %1};\n mov.b64 vv, {%2, %3};\n"
-        " mov.b64 ss, {%4, %4};\n fma.rn.f32x2 acc, ss, vv, acc;\n mov.b64 {%0, %1}, acc;\n}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(v0), "f"(v1), "f"(s));
 }
 
 // ---------------------------------------------------------------- tiles
@@ -398,7 +392,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
       } else if (warp == 1 || warp == 2) {
         // ------------------------------------------------------------ MMA issuers
         // Two issuers on two schedulers: group gi (its own accumulator buffer
-        // gi & 1, fresh at its first K step) is issued by warp 1 + (gi & 1).
+        // gi % kDBufs, fresh at its first K step) is issued by warp 1 + (gi & 1).
         // One issuing thread spent most of each stage on barrier and commit
         // latency next to the dequantiser and epilogue warps of its scheduler.
         const uint32_t me = (uint32_t)(warp - 1);
@@ -432,9 +426,9 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     const uint32_t a0 = tmem + (uint32_t)(ta * 64);
 #pragma unroll
                     for (int gg = 0; gg < kGroups; ++gg, ++gi) {
-                        const int b = gi & 1;
-                        if ((uint32_t)b != me) continue;
-                        if (!mbar_wait(bar(kBarDEmpty + b), ((gi >> 1) & 1) ^ 1, abort_flag, p.hdr)) {
+                        if ((gi & 1) != me) continue;
+                        const int b = gi % kDBufs;
+                        if (!mbar_wait(bar(kBarDEmpty + b), ((gi / kDBufs) & 1) ^ 1, abort_flag, p.hdr)) {
                             ok = false;
                             break;
                         }
@@ -521,7 +515,10 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         const int q = warp & 3;
         const int half = (warp - kEpilogueWarp0) >> 2;
         const int m = q * 32 + lane;
-        const int col0 = half * 64;
+        // 32-column blocks half and half + 2, so both warps of a quarter have work
+        // when a tile holds 33-96 tokens: acc[j] is column col(j)
+        const int col0 = half * 32;
+        auto col = [&](int j) { return j < 32 ? col0 + j : 64 + col0 + (j - 32); };
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         // gate+up: row m is gate (gu = 0) or up (gu = 1) row f_local of the band
         const int gu = (m >> 4) & 1;
@@ -541,17 +538,17 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.f;
             for (int g = 0; g < ti.ng; ++g, ++gi) {
-                const int b = gi & 1;
-                if (ok && !mbar_wait(bar(kBarDFull + b), (gi >> 1) & 1, abort_flag, p.hdr)) ok = false;
+                const int b = gi % kDBufs;
+                if (ok && !mbar_wait(bar(kBarDFull + b), (gi / kDBufs) & 1, abort_flag, p.hdr)) ok = false;
                 if (!ok) continue;
                 tc_fence_after();
                 const float s = __half2float(srow[g]);
                 const uint32_t dcol = tmem + lane_base + (uint32_t)(kTmemD + b * 128 + col0);
                 if (col0 < ti.npad) {
                     uint32_t v[64];
-                    const bool two = col0 + 32 < ti.npad;
+                    const bool two = 64 + col0 < ti.npad;
                     tmem_ld_x32(dcol, v);
-                    if (two) tmem_ld_x32(dcol + 32, v + 32);
+                    if (two) tmem_ld_x32(dcol + 64, v + 32);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                     for (int j = 0; j < 32; j += 2)
@@ -580,7 +577,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     const float other = __shfl_xor_sync(0xffffffffu, acc[j], 16);
                     const float gv = lo ? acc[j] : other;
                     const float uv = lo ? other : acc[j];
-                    const int nn = col0 + j;
+                    const int nn = col(j);
                     if (ok && lo == (j < 32) && nn < ti.n) {
                         const float hv = gv / (1.0f + expf(-gv)) * uv;
                         H[(int64_t)(ti.row0 + nn) * p.ld_out + f] = float_to_bf16_bits(hv);
@@ -590,7 +587,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 float* Y = reinterpret_cast<float*>(p.out);
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
-                    const int nn = col0 + j;
+                    const int nn = col(j);
                     if (nn < ti.n) Y[(int64_t)(ti.row0 + nn) * p.ld_out + 128 * ti.band + m] = acc[j];
                 }
             }

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(256) router_logits_sgemm(const uint16_t* __res
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int j = 0; j < 8; j += 2) ffma2(acc[i][j], acc[i][j + 1], av[i], bv[j], bv[j + 1]);
         }
         if (s + 1 < nsteps) store(buf ^ 1, xa, wb);
         __syncthreads();
