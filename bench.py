@@ -317,7 +317,7 @@ class GpuBench:
 DECODE1_TRAFFIC = 4_269_312 + 48_120_832 + 30_976 + 23_850_240
 
 
-def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms):
+def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
     """The decode step against HBM.  Algorithmic bytes = packed int4 weights + fp16 scales
     of the active routed experts and of the shared expert (gate+up and down), per step.
     The step is three launches (fused router, gate+up GEMV, down GEMV + combine) and the
@@ -327,7 +327,10 @@ def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms):
     achieved = nbytes / (ms * 1e-3) / 1e9
     peak = pk["hbm_gbs"]
     router_bytes = cfg.E * cfg.d * 4
-    return {"kernel": "decode step: router_decode_kernel + gateup_gemv_kernel + down_gemv_kernel",
+    kernel = ("decode step: router_decode_kernel + gateup_gemv_kernel + down_gemv_kernel"
+              if kernels_per_step(cfg, flags) == 3 else
+              "layer step on the grouped path (router, descriptors, gather, grouped GEMMs, combine)")
+    return {"kernel": kernel,
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": DECODE1_TRAFFIC if cfg.name == "decode1" else None,
@@ -497,7 +500,13 @@ def main():
                          f"{sec:.1f} s of single-thread CPU work"}
 
     if rank == 0:
-        roof = gpu_roofline_decode(cfg, ms, main_res["active"], pk, pk_kind, main_res["gu_ms"])
+        if cfg.T <= 64:  # decode: weight streaming against HBM, per step
+            roof = gpu_roofline_decode(cfg, ms, main_res["active"], pk, pk_kind, main_res["gu_ms"],
+                                       args.flags)
+        else:  # prefill: the gate+up grouped kernel against the dense bf16 peak
+            roof = gpu_roofline_prefill(cfg, main_res["gu_ms"], pk, pk_kind)
+            roof["layer_tflops"] = round(cfg.flops() / (ms * 1e-3) / 1e12, 2)
+            roof["layer_frac_of_bf16_peak"] = round(roof["layer_tflops"] / pk["bf16_tflops"], 4)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -526,7 +535,9 @@ def main():
         }
         if sec_res is not None:
             scfg = sec_res["cfg"]
-            sroof = gpu_roofline_prefill(scfg, sec_res["gu_ms"], pk, pk_kind)
+            sroof = (gpu_roofline_prefill(scfg, sec_res["gu_ms"], pk, pk_kind) if scfg.T > 64 else
+                     gpu_roofline_decode(scfg, sec_res["ms"], sec_res["active"], pk, pk_kind,
+                                         sec_res["gu_ms"]))
             tf = scfg.flops() / (sec_res["ms"] * 1e-3) / 1e12
             line["secondary"] = {
                 "workload": f"{scfg.name}: T={scfg.T}, same layer shapes, seed {scfg.seed}",

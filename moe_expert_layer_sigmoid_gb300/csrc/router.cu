@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) router_logits_gemv(const uint16_t* __rest
 // double-buffered shared memory filled from registers loaded one step ahead.
 // The K dimension is split over gridDim.z slices so that the grid covers the
 // GPU; the top-k sums the slices in order.
-constexpr int kSgBM = 128, kSgBN = 128, kSgBK = 8;
+constexpr int kSgBM = 128, kSgBN = 128, kSgBK = 16;
 
 __global__ void __launch_bounds__(256) router_logits_sgemm(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ W_r, int T,
@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(256) router_logits_sgemm(const uint16_t* __res
     const int e0 = blockIdx.x * kSgBN, t0 = blockIdx.y * kSgBM;
     const int kz = blockIdx.z, kbeg = kz * kchunk;
     const int tx = tid & 15, ty = tid >> 4;
-    // loader: row lr (token / expert) of the tile, 4 consecutive k at lk
-    const int lr = tid >> 1, lk = (tid & 1) * 4;
+    // loader: row lr (token / expert) of the tile, 8 consecutive k at lk
+    const int lr = tid >> 1, lk = (tid & 1) * 8;
     const int lt = t0 + lr, le = e0 + lr;
     float acc[8][8];
 #pragma unroll
@@ -57,23 +57,30 @@ __global__ void __launch_bounds__(256) router_logits_sgemm(const uint16_t* __res
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-    auto load = [&](int k, uint2& xa, float4& wb) {
-        xa = lt < T ? __ldg(reinterpret_cast<const uint2*>(x + (int64_t)lt * d + k + lk)) : make_uint2(0, 0);
-        wb = le < E ? __ldg(reinterpret_cast<const float4*>(W_r + (int64_t)le * d + k + lk))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    auto load = [&](int k, uint4& xa, float4* wb) {
+        xa = lt < T ? __ldg(reinterpret_cast<const uint4*>(x + (int64_t)lt * d + k + lk)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            wb[i] = le < E ? __ldg(reinterpret_cast<const float4*>(W_r + (int64_t)le * d + k + lk) + i)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
     };
-    auto store = [&](int buf, uint2 xa, float4 wb) {
-        As[buf][lk + 0][lr] = bf16_lo(xa.x);
-        As[buf][lk + 1][lr] = bf16_hi(xa.x);
-        As[buf][lk + 2][lr] = bf16_lo(xa.y);
-        As[buf][lk + 3][lr] = bf16_hi(xa.y);
-        Bs[buf][lk + 0][lr] = wb.x;
-        Bs[buf][lk + 1][lr] = wb.y;
-        Bs[buf][lk + 2][lr] = wb.z;
-        Bs[buf][lk + 3][lr] = wb.w;
+    auto store = [&](int buf, uint4 xa, const float4* wb) {
+        const uint32_t xw[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            As[buf][lk + 2 * i][lr] = bf16_lo(xw[i]);
+            As[buf][lk + 2 * i + 1][lr] = bf16_hi(xw[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            Bs[buf][lk + 4 * i + 0][lr] = wb[i].x;
+            Bs[buf][lk + 4 * i + 1][lr] = wb[i].y;
+            Bs[buf][lk + 4 * i + 2][lr] = wb[i].z;
+            Bs[buf][lk + 4 * i + 3][lr] = wb[i].w;
+        }
     };
-    uint2 xa;
-    float4 wb;
+    uint4 xa;
+    float4 wb[2];
     load(kbeg, xa, wb);
     store(0, xa, wb);
     __syncthreads();
