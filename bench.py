@@ -341,6 +341,11 @@ def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
             "peak_source": f"{pk_kind} hbm_gbs"}
 
 
+# DRAM bytes (read + write) of one gate+up launch at prefill2048 from one
+# `ncu --set full` capture of grouped_w4a16_kernel on this code (cold caches).
+PREFILL2048_GATEUP_TRAFFIC = 363_845_120 + 46_779_648
+
+
 def gpu_roofline_prefill(cfg, gu_ms, pk, pk_kind):
     """Gate+up kernel at prefill: algorithmic flops = 2 * (2F) * d per routed slot and per
     shared row."""
@@ -348,7 +353,8 @@ def gpu_roofline_prefill(cfg, gu_ms, pk, pk_kind):
     achieved = flops / (gu_ms * 1e-3) / 1e12
     peak = pk["bf16_tflops"]
     return {"kernel": "gateup", "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "traffic": PREFILL2048_GATEUP_TRAFFIC if cfg.name == "prefill2048" else None,
             "flops_per_launch": flops, "launch_us": round(gu_ms * 1e3, 2),
             "peak_source": f"{pk_kind} bf16_tflops"}
 
