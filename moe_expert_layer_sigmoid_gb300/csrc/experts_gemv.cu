@@ -638,8 +638,8 @@ __device__ __forceinline__ void dn_combine(const DnArgs& a, int q_lo, int nqc) {
 // its items are (group y, quad) group-major, group 0 being the shared expert
 // and group y > 0 the routed expert sched[y - 1]; warp w takes items w,
 // w + 16, ...  The routing is complete at launch (the gate+up kernel lets this
-// kernel launch only after its own wait for the router), so the first weights
-// are requested before the wait for H.  For T == 1 the token's H rows (k
+// kernel launch only after its own wait for the router), so the first two
+// items' weights are requested before the wait for H.  For T == 1 the token's H rows (k
 // routed + 1 shared) and their chunk sums are staged in shared memory.
 template <int CPL, bool ONE>
 __global__ void __launch_bounds__(kDnThreads, 1) down_gemv_kernel(const DnArgs a, int h_rows) {
@@ -664,9 +664,13 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_gemv_kernel(const DnArgs a
     };
     DnBuf<CPL> A, B;
     int e, c0;
-    if (n > 0) {
+    if (n > 0) {  // the first two items' weights do not depend on H
         next(&e, &c0);
         dn_load<CPL>(a, e, c0, lane, A);
+    }
+    if (n > 1) {
+        next(&e, &c0);
+        dn_load<CPL>(a, e, c0, lane, B);
     }
     pdl_wait();  // H is written by the gate+up kernel
     uint32_t hs = 0, hsum = 0;
@@ -683,16 +687,18 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_gemv_kernel(const DnArgs a
         hsum = (uint32_t)__cvta_generic_to_shared(sums);
     }
     for (int u = 0; u < n; u += 2) {
-        if (u + 1 < n) {
-            next(&e, &c0);
-            dn_load<CPL>(a, e, c0, lane, B);
-        }
         dn_compute<CPL, ONE>(a, A, hs, hsum, lane);
         if (u + 2 < n) {
             next(&e, &c0);
             dn_load<CPL>(a, e, c0, lane, A);
         }
-        if (u + 1 < n) dn_compute<CPL, ONE>(a, B, hs, hsum, lane);
+        if (u + 1 < n) {
+            dn_compute<CPL, ONE>(a, B, hs, hsum, lane);
+            if (u + 3 < n) {
+                next(&e, &c0);
+                dn_load<CPL>(a, e, c0, lane, B);
+            }
+        }
     }
     if (a.out) dn_combine(a, q_lo, nqc);
 }

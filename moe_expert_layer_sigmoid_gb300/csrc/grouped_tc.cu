@@ -208,6 +208,20 @@ __device__ __forceinline__ void nib8_to_bf16x2(uint32_t w, uint32_t* out) {
     }
 }
 
+// Same word, pairs (j, j + 4) instead: out[j] = {e_j, e_j+4}, one shift and one
+// lop3 per pair (no byte permute).  The contraction is unchanged if the other
+// operand stores each 8-element block in the matching order (x0, x4, x1, x5,
+// x2, x6, x3, x7), which gather_rows_kernel does for the gate+up activations.
+__device__ __forceinline__ void nib8_to_bf16x2_paired(uint32_t w, uint32_t* out) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t t, q;
+        asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(t) : "r"(w >> (4 * j)), "r"(0x000F000Fu), "r"(0x43084308u));
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(t), "r"(0x3F803F80u), "r"(0xC308C308u));
+        out[j] = q;
+    }
+}
+
 // ---------------------------------------------------------------- TMEM copies
 __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t* v) {
     asm volatile(
@@ -331,130 +345,130 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
     const int grid = gridDim.x;
 
     if (warp < kDequantWarp0) {
-      // each warpgroup changes its register count inside its own branch
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
-      if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            int tc = 0;
-            int4 cur = load_tile(p, blockIdx.x, n_tiles);
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid, ++tc) {
-                const int4 nxt = load_tile(p, tile + grid, n_tiles);  // one tile ahead
-                const TileInfo ti = decode_tile<G>(p, cur);
-                // the tile's scale block(s)
-                const int sb = tc & 1;
-                if (!mbar_wait(bar(kBarScEmpty + sb), ((tc >> 1) & 1) ^ 1, abort_flag, p.hdr)) {
-                    ok = false;
-                    break;
-                }
-                const __half* sbase_g = ti.grp >= 0 ? p.s_routed : p.s_shared;
-                const uint32_t scdst = sbase + kOffSc + sb * kScBytes;
-                if (p.mode == kGateUp) {
-                    const uint32_t blk_bytes = 64u * ti.ng * 2u;
-                    mbar_expect_tx(bar(kBarScFull + sb), 2 * blk_bytes);
-                    bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, blk_bytes,
-                              bar(kBarScFull + sb));
-                    bulk_load(scdst + blk_bytes, sbase_g + (int64_t)weight_row(p, ti, 1, 0) * ti.ng,
-                              blk_bytes, bar(kBarScFull + sb));
-                } else {
-                    const uint32_t bytes = 128u * ti.ng * 2u;
-                    mbar_expect_tx(bar(kBarScFull + sb), bytes);
-                    bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, bytes,
-                              bar(kBarScFull + sb));
-                }
-                const CUtensorMap* tma = ti.grp >= 0 ? &p.tm_a : &p.tm_a_sh;
-                const int nks = ti.K / kKStage;
-                for (int ks = 0; ks < nks; ++ks, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
-                    if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1, abort_flag, p.hdr)) { ok = false; break; }
-                    mbar_expect_tx(bar(kBarFull + s), (uint32_t)(kAStageBytes + kBStageBytes));
-                    // one box each: the weight tile and both 64-wide K blocks of the activations
-                    const uint32_t adst = sbase + kOffA + s * kAStageBytes;
-                    if (p.mode == kGateUp)  // rows m = 32*blk + 16*gu + i (gate/up interleaved)
-                        tma_load_5d(adst, tma, ks * 64, 0, 0, 4 * ti.band, ti.grp >= 0 ? ti.grp : 0,
+        // each warpgroup changes its register count inside its own branch
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
+        if (warp == 0) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                uint32_t it = 0;
+                bool ok = true;
+                int tc = 0;
+                int4 cur = load_tile(p, blockIdx.x, n_tiles);
+                for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid, ++tc) {
+                    const int4 nxt = load_tile(p, tile + grid, n_tiles);  // one tile ahead
+                    const TileInfo ti = decode_tile<G>(p, cur);
+                    // the tile's scale block(s)
+                    const int sb = tc & 1;
+                    if (!mbar_wait(bar(kBarScEmpty + sb), ((tc >> 1) & 1) ^ 1, abort_flag, p.hdr)) {
+                        ok = false;
+                        break;
+                    }
+                    const __half* sbase_g = ti.grp >= 0 ? p.s_routed : p.s_shared;
+                    const uint32_t scdst = sbase + kOffSc + sb * kScBytes;
+                    if (p.mode == kGateUp) {
+                        const uint32_t blk_bytes = 64u * ti.ng * 2u;
+                        mbar_expect_tx(bar(kBarScFull + sb), 2 * blk_bytes);
+                        bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, blk_bytes,
+                                  bar(kBarScFull + sb));
+                        bulk_load(scdst + blk_bytes, sbase_g + (int64_t)weight_row(p, ti, 1, 0) * ti.ng,
+                                  blk_bytes, bar(kBarScFull + sb));
+                    } else {
+                        const uint32_t bytes = 128u * ti.ng * 2u;
+                        mbar_expect_tx(bar(kBarScFull + sb), bytes);
+                        bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, bytes,
+                                  bar(kBarScFull + sb));
+                    }
+                    const CUtensorMap* tma = ti.grp >= 0 ? &p.tm_a : &p.tm_a_sh;
+                    const int nks = ti.K / kKStage;
+                    for (int ks = 0; ks < nks; ++ks, ++it) {
+                        const int s = it % kStages;
+                        const uint32_t ph = (it / kStages) & 1;
+                        if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1, abort_flag, p.hdr)) { ok = false; break; }
+                        mbar_expect_tx(bar(kBarFull + s), (uint32_t)(kAStageBytes + kBStageBytes));
+                        // one box each: the weight tile and both 64-wide K blocks of the activations
+                        const uint32_t adst = sbase + kOffA + s * kAStageBytes;
+                        if (p.mode == kGateUp)  // rows m = 32*blk + 16*gu + i (gate/up interleaved)
+                            tma_load_5d(adst, tma, ks * 64, 0, 0, 4 * ti.band, ti.grp >= 0 ? ti.grp : 0,
+                                        bar(kBarFull + s));
+                        else
+                            tma_load_2d(adst, tma, ks * 64, weight_row(p, ti, 0, 0), bar(kBarFull + s));
+                        tma_load_3d(sbase + kOffB + s * kBStageBytes, &p.tm_b, 0, ti.row0, 2 * ks,
                                     bar(kBarFull + s));
-                    else
-                        tma_load_2d(adst, tma, ks * 64, weight_row(p, ti, 0, 0), bar(kBarFull + s));
-                    tma_load_3d(sbase + kOffB + s * kBStageBytes, &p.tm_b, 0, ti.row0, 2 * ks,
-                                bar(kBarFull + s));
-                }
-                cur = nxt;
-            }
-            // do not leave with copies in flight
-            if (!ok)
-                for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j)
-                    mbar_wait(bar(kBarFull + j % kStages), (j / kStages) & 1, abort_flag, p.hdr);
-        }
-        __syncwarp();
-      } else if (warp == 1 || warp == 2) {
-        // ------------------------------------------------------------ MMA issuers
-        // Two issuers on two schedulers: group gi (its own accumulator buffer
-        // gi % kDBufs, fresh at its first K step) is issued by warp 1 + (gi & 1).
-        // One issuing thread spent most of each stage on barrier and commit
-        // latency next to the dequantiser and epilogue warps of its scheduler.
-        const uint32_t me = (uint32_t)(warp - 1);
-        if (lane == 0) {
-            uint32_t it = 0, gi = 0;
-            int64_t last = -1;  // last stage this issuer committed
-            bool ok = true;
-            int4 cur = load_tile(p, blockIdx.x, n_tiles);
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
-                const int4 nxt = load_tile(p, tile + grid, n_tiles);
-                const TileInfo ti = decode_tile<G>(p, cur);
-                const uint32_t idesc = idesc_bf16(128, ti.npad);
-                const int nks = ti.K / kKStage;
-                for (int ks = 0; ks < nks && ok; ++ks, ++it) {
-                    const int s = it % kStages;
-                    const int ta = it % kAStagesT;
-                    const uint32_t tph = (it / kAStagesT) & 1;
-                    constexpr int kGroups = kKStage / G;
-                    if (kGroups == 1 && (gi & 1) != me) {  // the other issuer's stage
-                        ++gi;
-                        continue;
                     }
-                    // AREADY completes only after every dequantiser warp has seen FULL for
-                    // this stage (A and B land on the same barrier), so it also orders the
-                    // B tile before the MMAs
-                    if (!mbar_wait(bar(kBarAReady + ta), tph, abort_flag, p.hdr)) { ok = false; break; }
-                    tc_fence_after();
-                    // descriptor of the stage's B tile; K steps add (kg/4)*16 KB + (kg%4)*32 B,
-                    // i.e. (kg/4)*1024 + (kg%4)*2 in the 16-byte address field
-                    const uint64_t bdesc0 = smem_desc_sw128(sbase + kOffB + s * kBStageBytes);
-                    const uint32_t a0 = tmem + (uint32_t)(ta * 64);
-#pragma unroll
-                    for (int gg = 0; gg < kGroups; ++gg, ++gi) {
-                        if ((gi & 1) != me) continue;
-                        const int b = gi % kDBufs;
-                        if (!mbar_wait(bar(kBarDEmpty + b), ((gi / kDBufs) & 1) ^ 1, abort_flag, p.hdr)) {
-                            ok = false;
-                            break;
+                    cur = nxt;
+                }
+                // do not leave with copies in flight
+                if (!ok)
+                    for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j)
+                        mbar_wait(bar(kBarFull + j % kStages), (j / kStages) & 1, abort_flag, p.hdr);
+            }
+            __syncwarp();
+        } else if (warp == 1 || warp == 2) {
+            // ------------------------------------------------------------ MMA issuers
+            // Two issuers on two schedulers: group gi (its own accumulator buffer
+            // gi % kDBufs, fresh at its first K step) is issued by warp 1 + (gi & 1).
+            // One issuing thread spent most of each stage on barrier and commit
+            // latency next to the dequantiser and epilogue warps of its scheduler.
+            const uint32_t me = (uint32_t)(warp - 1);
+            if (lane == 0) {
+                uint32_t it = 0, gi = 0;
+                int64_t last = -1;  // last stage this issuer committed
+                bool ok = true;
+                int4 cur = load_tile(p, blockIdx.x, n_tiles);
+                for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
+                    const int4 nxt = load_tile(p, tile + grid, n_tiles);
+                    const TileInfo ti = decode_tile<G>(p, cur);
+                    const uint32_t idesc = idesc_bf16(128, ti.npad);
+                    const int nks = ti.K / kKStage;
+                    for (int ks = 0; ks < nks && ok; ++ks, ++it) {
+                        const int s = it % kStages;
+                        const int ta = it % kAStagesT;
+                        const uint32_t tph = (it / kAStagesT) & 1;
+                        constexpr int kGroups = kKStage / G;
+                        if (kGroups == 1 && (gi & 1) != me) {  // the other issuer's stage
+                            ++gi;
+                            continue;
                         }
+                        // AREADY completes only after every dequantiser warp has seen FULL for
+                        // this stage (A and B land on the same barrier), so it also orders the
+                        // B tile before the MMAs
+                        if (!mbar_wait(bar(kBarAReady + ta), tph, abort_flag, p.hdr)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t dcol = tmem + (uint32_t)(kTmemD + b * 128);
-#pragma unroll
-                        for (int kk = 0; kk < G / 16; ++kk) {
-                            const int kg = gg * (G / 16) + kk;  // 16-wide K step within the stage
-                            mma_ts(dcol, a0 + (uint32_t)(kg * 8),
-                                   bdesc0 + (uint64_t)((kg >> 2) * 1024 + (kg & 3) * 2), idesc,
-                                   kk > 0 ? 1u : 0u);
+                        // descriptor of the stage's B tile; K steps add (kg/4)*16 KB + (kg%4)*32 B,
+                        // i.e. (kg/4)*1024 + (kg%4)*2 in the 16-byte address field
+                        const uint64_t bdesc0 = smem_desc_sw128(sbase + kOffB + s * kBStageBytes);
+                        const uint32_t a0 = tmem + (uint32_t)(ta * 64);
+    #pragma unroll
+                        for (int gg = 0; gg < kGroups; ++gg, ++gi) {
+                            if ((gi & 1) != me) continue;
+                            const int b = gi % kDBufs;
+                            if (!mbar_wait(bar(kBarDEmpty + b), ((gi / kDBufs) & 1) ^ 1, abort_flag, p.hdr)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t dcol = tmem + (uint32_t)(kTmemD + b * 128);
+    #pragma unroll
+                            for (int kk = 0; kk < G / 16; ++kk) {
+                                const int kg = gg * (G / 16) + kk;  // 16-wide K step within the stage
+                                mma_ts(dcol, a0 + (uint32_t)(kg * 8),
+                                       bdesc0 + (uint64_t)((kg >> 2) * 1024 + (kg & 3) * 2), idesc,
+                                       kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(bar(kBarDFull + b));
                         }
-                        mma_commit(bar(kBarDFull + b));
+                        if (!ok) break;
+                        mma_commit(bar(kBarEmpty + s));
+                        last = it;
                     }
-                    if (!ok) break;
-                    mma_commit(bar(kBarEmpty + s));
-                    last = it;
+                    cur = nxt;
                 }
-                cur = nxt;
+                // this issuer's last commit has landed before the CTA can exit
+                if (ok && last >= 0)
+                    mbar_wait(bar(kBarEmpty + last % kStages), (uint32_t)(last / kStages) & 1, abort_flag, p.hdr);
             }
-            // this issuer's last commit has landed before the CTA can exit
-            if (ok && last >= 0)
-                mbar_wait(bar(kBarEmpty + last % kStages), (uint32_t)(last / kStages) & 1, abort_flag, p.hdr);
+            __syncwarp();
         }
-        __syncwarp();
-      }
     } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------------ dequantisers
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegDq));
@@ -483,12 +497,22 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarEmpty + s));
                 uint32_t r[32];
+                if (p.mode == kGateUp) {  // activations stored block-permuted
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    nib8_to_bf16x2(v[c].x, r + 16 * c + 0);
-                    nib8_to_bf16x2(v[c].y, r + 16 * c + 4);
-                    nib8_to_bf16x2(v[c].z, r + 16 * c + 8);
-                    nib8_to_bf16x2(v[c].w, r + 16 * c + 12);
+                    for (int c = 0; c < 2; ++c) {
+                        nib8_to_bf16x2_paired(v[c].x, r + 16 * c + 0);
+                        nib8_to_bf16x2_paired(v[c].y, r + 16 * c + 4);
+                        nib8_to_bf16x2_paired(v[c].z, r + 16 * c + 8);
+                        nib8_to_bf16x2_paired(v[c].w, r + 16 * c + 12);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        nib8_to_bf16x2(v[c].x, r + 16 * c + 0);
+                        nib8_to_bf16x2(v[c].y, r + 16 * c + 4);
+                        nib8_to_bf16x2(v[c].z, r + 16 * c + 8);
+                        nib8_to_bf16x2(v[c].w, r + 16 * c + 12);
+                    }
                 }
                 const int ta = it % kAStagesT;
                 if (it >= kAStagesT) {  // TMEM stage ta is free once the MMAs of stage it - kAStagesT are done
@@ -606,8 +630,10 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
 }
 
 // Gate+up activation rows in descriptor order: xs[r] = x[perm[r] / k] for the
-// T*k routed rows, then xs[T*k + t] = x[t] for the shared expert.  One warp
-// per row, 16-byte copies.
+// T*k routed rows, then xs[T*k + t] = x[t] for the shared expert.  Each
+// 8-element block is stored as (x0, x4, x1, x5, x2, x6, x3, x7), the order of
+// the dequantiser's weight pairs (nib8_to_bf16x2_paired).  One warp per row,
+// 16-byte copies.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm, int T,
                                                           int k, int d, uint16_t* __restrict__ xs) {
@@ -617,7 +643,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
     const int64_t t = r < slots ? __ldg(perm + r) / k : r - slots;
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
     uint4* dst = reinterpret_cast<uint4*>(xs + r * d);
-    for (int c = threadIdx.x & 31; c < d / 8; c += 32) dst[c] = __ldg(src + c);
+    for (int c = threadIdx.x & 31; c < d / 8; c += 32) {
+        const uint4 v = __ldg(src + c);
+        uint4 o;
+        o.x = __byte_perm(v.x, v.z, 0x5410);
+        o.y = __byte_perm(v.x, v.z, 0x7632);
+        o.z = __byte_perm(v.y, v.w, 0x5410);
+        o.w = __byte_perm(v.y, v.w, 0x7632);
+        dst[c] = o;
+    }
 }
 
 // ---------------------------------------------------------------- host side
