@@ -418,6 +418,18 @@ def oracle_sample(cfg, budget_s: float, max_tokens: int):
 
 # ---------------------------------------------------------------- main
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest of a per-rank value over the process group (the slowest rank's step time
+    sets the job's throughput); the value itself when no group is initialised."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -490,11 +502,7 @@ def main():
     if args.secondary and args.secondary != args.config:
         sec_res = measure_config(args.secondary, device, args.warmup, args.secondary_steps,
                                  args.ncopy, args.nbatch, pk, pk_kind, gpu_index)
-    ms = main_res["ms"]
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(main_res["ms"], device)
     cfg = main_res["cfg"]
     value = world * cfg.T / (ms * 1e-3)
 
