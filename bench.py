@@ -343,7 +343,7 @@ def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
 
 # DRAM bytes (read + write) of one gate+up launch at prefill2048 from one
 # `ncu --set full` capture of grouped_w4a16_kernel on this code (cold caches).
-PREFILL2048_GATEUP_TRAFFIC = 363_845_120 + 46_779_648
+PREFILL2048_GATEUP_TRAFFIC = 363_650_816 + 46_725_120
 
 
 def gpu_roofline_prefill(cfg, gu_ms, pk, pk_kind):
