@@ -48,12 +48,13 @@
 namespace moe {
 namespace {
 
-// Gate+up: 12 warps at up to 112 registers (43K of the 64K-register file), so
-// a CTA fits beside the decode router's last CTA and every CTA is resident
-// (and has its shared-expert rows in flight) when the routing lands.
-// Down: 16 warps.
-constexpr int kGuWarps = 12;
-constexpr int kGuThreads = kGuWarps * 32;
+// Warps per gate+up CTA: 16 for one token (112 registers, 57K of the 64K
+// register file), 12 for several (160 registers: the multi-token passes keep
+// more values live).  At T = 1 the 16-warp CTA cannot sit beside the decode
+// router's last CTA, so the one on that SM starts when the router ends; the
+// extra loads in flight on every other SM outweigh that (measured 17.2 against
+// 18.4 us for the launch, 35.8 against 37.0 us for the step).  Down: 16 warps.
+__host__ __device__ constexpr int gu_warps(bool one) { return one ? 16 : 12; }
 constexpr int kDnWarps = 16;
 constexpr int kDnThreads = kDnWarps * 32;
 constexpr int kGuTokPass = 4;  // tokens per pass of the gate+up kernel (T > 1)
@@ -440,6 +441,7 @@ __global__ void __maxnreg__(ONE ? 112 : 160) gateup_gemv_kernel(const GuArgs a) 
     {   // the shared expert reads only x: it runs before the wait for the router
         const int lo = (int)((int64_t)b * a.Fs / G), hi = (int)((int64_t)(b + 1) * a.Fs / G);
         const int first = lo + warp;
+        constexpr int kGuWarps = gu_warps(ONE);
         const int n = first < hi ? (hi - first + kGuWarps - 1) / kGuWarps : 0;
         gu_pipeline<CPL, ONE>(
             a, n,
@@ -455,6 +457,7 @@ __global__ void __maxnreg__(ONE ? 112 : 160) gateup_gemv_kernel(const GuArgs a) 
     const int64_t R = (int64_t)n_act * a.F;
     const int64_t lo = (int64_t)b * R / G, hi = (int64_t)(b + 1) * R / G;
     const int64_t first = lo + warp;
+    constexpr int kGuWarps = gu_warps(ONE);
     const int n = first < hi ? (int)((hi - first + kGuWarps - 1) / kGuWarps) : 0;
     // cursor (group, row) in load order
     int cy = n ? (int)(first / a.F) : 0;
@@ -742,8 +745,8 @@ cudaError_t launch_persistent(Kern kern, int threads, size_t smem, bool pdl, cud
 template <int CPL>
 cudaError_t launch_gu(const GuArgs& a, bool one, bool pdl, cudaStream_t st) {
     const size_t smem = one ? (size_t)CPL * 4 * 32 * 16 : 0;
-    return one ? launch_persistent(gateup_gemv_kernel<CPL, true>, kGuThreads, smem, pdl, st, a)
-               : launch_persistent(gateup_gemv_kernel<CPL, false>, kGuThreads, smem, pdl, st, a);
+    return one ? launch_persistent(gateup_gemv_kernel<CPL, true>, gu_warps(true) * 32, smem, pdl, st, a)
+               : launch_persistent(gateup_gemv_kernel<CPL, false>, gu_warps(false) * 32, smem, pdl, st, a);
 }
 
 template <int CPL>
