@@ -314,7 +314,7 @@ class GpuBench:
 # DRAM bytes (read + write) per step of the decode chain at decode1, summed over
 # router_decode_kernel, gateup_gemv_kernel and down_gemv_kernel from one
 # `ncu --set full` capture of each on this code (cold caches).
-DECODE1_TRAFFIC = 4_269_312 + 48_120_832 + 30_976 + 23_851_264
+DECODE1_TRAFFIC = 4_269_312 + 48_279_552 + 27_392 + 23_851_264
 
 
 def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
