@@ -19,7 +19,7 @@
 // Loads.  Each lane reads 16 bytes (32 nibbles, one quantisation-group scale)
 // per load, the 32 lanes of a warp a contiguous 512 bytes, straight into
 // registers; every warp loads its next item while it computes the current one
-// (two register buffers), so each SM keeps about 50 KB of reads in flight.
+// (two register buffers), so each SM keeps about 64 KB of reads in flight.
 // Streaming from HBM this way measured ~6.2 TB/s on GB300, against ~4 TB/s
 // for the same bytes moved by cp.async.bulk in 8-16 KB pieces.  For T = 1 the
 // token's x (and its 32-element chunk sums) sit in shared memory,
@@ -28,7 +28,7 @@
 // Launch order (programmatic dependent launch): the gate+up kernel requests
 // its shared-expert stages and loads x before it waits for the router, and
 // lets the down kernel launch once the routing is complete; the down kernel
-// requests its first weight stages before it waits for H.
+// requests its first two items' weights before it waits for H.
 //
 // Arithmetic.  Decode streams about two int4 weights per HBM byte, so the
 // kernel has only a few lane-operations per weight.  One lop3 turns bits 0-3

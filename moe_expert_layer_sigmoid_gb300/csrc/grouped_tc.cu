@@ -38,9 +38,12 @@
 //               fp32 registers (packed f32x2 FMAs); at the end of a tile apply
 //               SwiGLU (gate+up) or store Y (down)
 //
-// One dequantiser warp per quarter was the bound (a stage's 128 x 128 int4
-// tile took it ~900 cycles, latency-bound, against ~550 for the stage's
-// MMAs); two halve its share.
+// Two dequantisers per quarter keep the conversion ahead of the MMAs (one
+// took ~900 cycles per stage, latency-bound, against ~550 of tensor time).
+// Two MMA issuers on two schedulers hide each other's barrier and commit
+// latency; each TMEM A slot is used by every second stage, so splitting the
+// stages by parity gives every AREADY barrier a single waiter that consumes its
+// phases in order (a parity wait cannot tell phase k from phase k - 2).
 //
 // Numerics: each group's partial sum is sum_k x_k * q_k with exact bf16
 // products and fp32 accumulation; multiplying by the fp16 scale s in fp32
