@@ -35,12 +35,29 @@ def test_reference_arm_prints_one_contract_line():
         assert key in d, key
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC
     assert d["unit"] == "tokens/s" and d["higher_is_better"] is True and d["value"] > 0
-    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["steps_timed"] == 1
     assert d["config"]["workload"].startswith("decode1")
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] == d["value"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_is_bounded_in_time(monkeypatch):
+    """Whatever --steps is, the oracle work stops at REF_BUDGET_S."""
+    calls = []
+
+    def fake_sample(cfg, budget_s, max_tokens):
+        calls.append((budget_s, max_tokens))
+        return max(1, min(max_tokens, 3)), 0.5
+
+    monkeypatch.setattr(bench, "oracle_sample", fake_sample)
+
+    class A:
+        config, steps, warmup = "decode1", 40000, 10
+
+    assert bench.run_reference(A) == 0
+    assert calls[-1] == (bench.REF_BUDGET_S, 40000) and bench.REF_BUDGET_S <= 180
 
 
 def test_warmup_below_three_is_refused():
