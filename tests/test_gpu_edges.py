@@ -30,6 +30,7 @@ EDGE_CONFIGS = [
     (8, 768, 32, 8, 128, 384, 128),
     (1, 2048, 16, 16, 256, 128, 128),    # k == E at T = 1
     (7, 4096, 32, 10, 1024, 1024, 128),  # decode shapes, several tokens per expert
+    (9, 256, 1024, 32, 128, 128, 32),    # the largest E and k the library accepts
 ]
 
 
