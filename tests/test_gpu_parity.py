@@ -120,6 +120,24 @@ def test_layer_forward_matches_oracle(C):
     assert ok
 
 
+def test_host_buffer_forward_matches_device_forward(C):
+    """moe_layer_forward_host (pinned host x and out, copies on the stream) gives the same
+    bits as moe_layer_forward on device buffers, on a reused workspace."""
+    if C.cfg.T > 2048:
+        pytest.skip("the host-buffer path is the same code; 2048 tokens cover it")
+    dev = C.dev
+    dims = dev.dims()
+    ref, _ = forward(C)
+    ws = moe.workspace(moe.moe_layer_workspace_bytes(dims))
+    x_host = dev.x.cpu().pin_memory()
+    out_host = torch.empty((C.cfg.T, C.cfg.d), dtype=torch.int16).pin_memory()
+    for _ in range(2):
+        out_host.fill_(0)
+        moe.moe_layer_forward_host(x_host, dev.W_r, dev.bias, dims, *dev.w4s(), out_host, ws)
+        assert moe.moe_check_device_status(ws) == moe.MOE_OK
+        assert np.array_equal(out_host.numpy().view(np.uint16), ref)
+
+
 def test_stepwise_calls_match_forward_and_oracle_h(C):
     """The six per-step calls in sequence reproduce moe_layer_forward bit for bit;
     H rows of the sampled tokens match the oracle's h."""
