@@ -138,6 +138,44 @@ def test_host_buffer_forward_matches_device_forward(C):
         assert np.array_equal(out_host.numpy().view(np.uint16), ref)
 
 
+def test_graph_replay_matches_eager(C):
+    """moe_layer_forward captured in a CUDA graph (the bench's timing mode; the decode chain's
+    programmatic dependent launches included) replays to the eager bits, also after the
+    input is changed in place."""
+    if C.cfg.T > 2048:
+        pytest.skip("the capture is the same code; 2048 tokens cover it")
+    dev = C.dev
+    dims = dev.dims()
+
+    def eager(x):
+        ws = moe.workspace(moe.moe_layer_workspace_bytes(dims))
+        o = torch.empty((C.cfg.T, C.cfg.d), dtype=torch.int16, device="cuda")
+        moe.moe_layer_forward(x, dev.W_r, dev.bias, dims, *dev.w4s(), o, ws)
+        assert moe.moe_check_device_status(ws) == moe.MOE_OK
+        return o.clone()
+
+    x = dev.x.clone()
+    x2 = torch.flip(dev.x, dims=[0]).contiguous()
+    ref, ref2 = eager(x), eager(x2)
+    ws = moe.workspace(moe.moe_layer_workspace_bytes(dims))
+    out = torch.empty_like(ref)
+    moe.moe_layer_forward(x, dev.W_r, dev.bias, dims, *dev.w4s(), out, ws)  # warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.moe_layer_forward(x, dev.W_r, dev.bias, dims, *dev.w4s(), out, ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    x.copy_(x2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref2)
+    assert moe.moe_check_device_status(ws) == moe.MOE_OK
+
+
 def test_stepwise_calls_match_forward_and_oracle_h(C):
     """The six per-step calls in sequence reproduce moe_layer_forward bit for bit;
     H rows of the sampled tokens match the oracle's h."""
