@@ -23,8 +23,8 @@ EDGE_CONFIGS = [
     (65, 512, 40, 5, 128, 128, 128),     # just above the GEMV limit
     (130, 256, 16, 1, 256, 128, 32),     # k = 1, ragged token tiles
     (300, 768, 64, 6, 384, 256, 128),    # several 128-token tiles + ragged tail
-    # the tensor-core decode GEMV (group 128, T <= 8): K splits of 1-16 slices,
-    # 1-3 chunks per slice, F != F_s, partial MMA columns
+    # decode-sized batches at group 128: F != F_s, k == E, several tokens
+    # per expert, K from 512 to 4096
     (2, 512, 24, 3, 256, 128, 128),
     (5, 1024, 40, 4, 384, 256, 128),
     (8, 768, 32, 8, 128, 384, 128),
