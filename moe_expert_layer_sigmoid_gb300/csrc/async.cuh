@@ -70,11 +70,4 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
-// Order this thread's earlier generic-proxy accesses to shared memory before
-// later async-proxy (bulk copy) accesses, e.g. before refilling a buffer that
-// was just read with plain loads.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 }  // namespace moe

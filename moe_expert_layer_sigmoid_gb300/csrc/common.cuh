@@ -27,9 +27,8 @@ struct WsHeader {
     int32_t error_flags;   // OR of kErr* bits; cleared by moe_check_device_status
     int32_t n_active;      // routed experts with count > 0 (written by the descriptors)
     int32_t n_tiles[2];    // grouped-GEMM tile counts: [0] gate+up, [1] down
-    int32_t queue[4];      // work-queue counters of persistent kernels (reset per batch)
-    int32_t done[4];       // completion counters (reset by their last user)
-    int32_t pad[52];
+    int32_t done[4];       // arrival counters; [0]: CTAs of router_decode_kernel (the last resets it)
+    int32_t pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -59,7 +58,6 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Router tiling: T <= kRouterSmallT uses the split-K GEMV form.
 constexpr int kRouterSmallT = 64;
-constexpr int kRouterKChunk = 1024;
 
 // GEMV (decode) expert path by default for T <= kGemvMaxT (the CUDA-core GEMV
 // redoes its dequantisation per 4-token pass and is FMA-bound beyond a few
@@ -148,9 +146,6 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 
 // ---------------------------------------------------------------------------
 // Small device helpers.
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
-    return __uint_as_float(bits16 << 16);
-}
 __device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t pair) {
     return __uint_as_float(pair & 0xFFFF0000u);
@@ -159,8 +154,6 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
     __nv_bfloat16 b = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&b);
 }
-
-__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
 // a0 += s * v0, a1 += s * v1 as one packed f32x2 FMA (sm_100 family); each
 // lane rounds exactly as fmaf, so results match the scalar form bit for bit.
