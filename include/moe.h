@@ -70,7 +70,8 @@ typedef enum {
 
 /* Layer dimensions.  Supported: d % 256 == 0, F % 128 == 0, F_s % 128 == 0,
    group in {32, 64, 128} dividing d, F and F_s, 1 <= k <= min(E, 32),
-   1 <= E <= 1024, 0 <= T and T * (k + 1) < 2^31. */
+   1 <= E <= 1024, 0 <= T, T * (k + 1) < 2^31, and E * 2F < 2^31 and
+   E * d < 2^31 (the routed weight tensors' row counts). */
 typedef struct {
     int32_t T;      /* tokens in the batch                      */
     int32_t d;      /* model width                              */

@@ -118,6 +118,10 @@ moe_status_t check_dims(const moe_dims_t* d) {
     if (d->d % 256 || d->F % 128 || d->F_s % 128) return MOE_ERR_UNSUPPORTED;
     if (d->d % d->group || d->F % d->group || d->F_s % d->group) return MOE_ERR_UNSUPPORTED;
     if (d->k > 32 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
+    // Weight-row indices are 32-bit (the grouped kernel's TMA row coordinates):
+    // the routed gate+up tensor has E * 2F rows, the down tensor E * d.
+    if ((int64_t)d->E * 2 * d->F >= (int64_t)1 << 31 || (int64_t)d->E * d->d >= (int64_t)1 << 31)
+        return MOE_ERR_UNSUPPORTED;
     if ((d->flags & MOE_FLAG_FORCE_GEMV) && (d->flags & MOE_FLAG_FORCE_GROUPED))
         return MOE_ERR_INVALID_ARG;
     return MOE_OK;

@@ -53,6 +53,11 @@ def test_workspace_bytes(L):
     assert moe.moe_workspace_bytes(_dims(T=4096)) > a
     assert moe.moe_workspace_bytes(_dims(group=48)) == 0
     assert moe.moe_workspace_bytes(_dims(k=17, E=16)) == 0
+    # weight-row counts E * 2F and E * d must stay below 2^31
+    assert moe.moe_workspace_bytes(_dims(E=1024, k=4, F=(1 << 20) - 128)) > 0
+    assert moe.moe_workspace_bytes(_dims(E=1024, k=4, F=1 << 20)) == 0
+    assert moe.moe_workspace_bytes(_dims(E=1024, k=4, d=(1 << 21) - 256)) > 0
+    assert moe.moe_workspace_bytes(_dims(E=1024, k=4, d=1 << 21)) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -65,6 +70,8 @@ def test_workspace_bytes(L):
     (dict(E=2048, k=4), moe.MOE_ERR_UNSUPPORTED),
     (dict(T=-1), moe.MOE_ERR_INVALID_ARG),
     (dict(flags=3), moe.MOE_ERR_INVALID_ARG),
+    (dict(E=1024, k=4, F=1 << 20), moe.MOE_ERR_UNSUPPORTED),   # E * 2F = 2^31 weight rows
+    (dict(E=1024, k=4, d=1 << 21), moe.MOE_ERR_UNSUPPORTED),   # E * d = 2^31 weight rows
 ])
 def test_dims_validation(L, kw, code):
     d = _dims(**kw)
