@@ -58,7 +58,7 @@ def _get():
         "orc_descriptors": [p, i64, i32, i32, p, p, p, p, p],
         "orc_expert_token": [p, i32, i32, i32, p, p, p, p, p, p],
         "orc_layer_tokens": [p, i32, i32, i32, i32, i32, i32, p, p, p, p, p, p, p, p, p, p, p,
-                             i64, p, p, p],
+                             p, i64, p, p, p],
         "orc_f32_to_f16_array": [p, i64, p],
         "orc_f16_to_f32_array": [p, i64, p],
         "orc_f32_to_bf16_array": [p, i64, p],
@@ -266,10 +266,14 @@ def _map(fn, items, threads):
 
 
 def layer_tokens(x, W: PackedLayer, topk_idx, topk_w, tokens, threads: int = 1,
-                 want_h: bool = False):
+                 want_h: bool = False, residual=None):
     """Layer output for the listed tokens.  Returns (out bf16 bits [n][d],
-    h_routed [n][k][F] or None, h_shared [n][Fs] or None)."""
+    h_routed [n][k][F] or None, h_shared [n][Fs] or None).  ``residual``
+    (bf16 bits [T][d], optional) is added after the routed + shared sum."""
     x = np.ascontiguousarray(x, np.uint16)
+    if residual is not None:
+        residual = np.ascontiguousarray(residual, np.uint16)
+        assert residual.shape == x.shape
     topk_idx = np.ascontiguousarray(topk_idx, np.int32)
     topk_w = np.ascontiguousarray(topk_w, np.float32)
     tokens = np.ascontiguousarray(tokens, np.int64)
@@ -287,7 +291,7 @@ def layer_tokens(x, W: PackedLayer, topk_idx, topk_w, tokens, threads: int = 1,
         lib.orc_layer_tokens(
             _p(x), d, W.E, k, W.F, W.Fs, W.group, _p(topk_idx), _p(topk_w),
             _p(W.q_gu), _p(W.s_gu), _p(W.q_dn), _p(W.s_dn),
-            _p(W.qs_gu), _p(W.ss_gu), _p(W.qs_dn), _p(W.ss_dn),
+            _p(W.qs_gu), _p(W.ss_gu), _p(W.qs_dn), _p(W.ss_dn), _p(residual),
             tokens.ctypes.data + a * 8, b - a,
             out.ctypes.data + a * d * 2,
             None if h_r is None else h_r.ctypes.data + a * k * W.F * 2,
@@ -303,11 +307,14 @@ def layer_tokens(x, W: PackedLayer, topk_idx, topk_w, tokens, threads: int = 1,
     return out, h_r, h_s
 
 
-def layer(x, W_r, bias, W: PackedLayer, k: int, threads: int = 1, want_h: bool = False):
-    """The whole layer on every token: router, descriptors, experts, combine."""
+def layer(x, W_r, bias, W: PackedLayer, k: int, threads: int = 1, want_h: bool = False,
+          residual=None):
+    """The whole layer on every token: router, descriptors, experts, combine
+    (plus the residual row when given)."""
     idx, w, margin, _ = router(x, W_r, bias, k, threads=threads)
     desc = descriptors(idx, W.E)
     T = x.shape[0]
-    out, h_r, h_s = layer_tokens(x, W, idx, w, np.arange(T), threads=threads, want_h=want_h)
+    out, h_r, h_s = layer_tokens(x, W, idx, w, np.arange(T), threads=threads, want_h=want_h,
+                                 residual=residual)
     return dict(topk_idx=idx, topk_w=w, margin=margin, out=out, h_routed=h_r, h_shared=h_s,
                 **desc)

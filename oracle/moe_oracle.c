@@ -46,6 +46,10 @@
  *  R8 descriptors: perm lists slot ids t*k + j sorted by (expert, token);
  *     pos is its inverse; sched orders experts by count, largest first, ties
  *     to the lower id.
+ *  R9 residual add (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
+ *     residual + routed + shared in one launch, routed and shared summed
+ *     first): with a residual row r (bf16), out = bf16(float(r) + acc), where
+ *     acc is the fp32 routed + shared sum of R5, rounded once.
  */
 #include "moe_oracle.h"
 
@@ -297,8 +301,9 @@ void orc_layer_tokens(const uint16_t* x, int32_t d, int32_t E, int32_t k, int32_
                       int32_t group, const int32_t* topk_idx, const float* topk_w,
                       const uint8_t* q_gu, const uint16_t* s_gu, const uint8_t* q_dn,
                       const uint16_t* s_dn, const uint8_t* qs_gu, const uint16_t* ss_gu,
-                      const uint8_t* qs_dn, const uint16_t* ss_dn, const int64_t* tokens,
-                      int64_t n_tokens, uint16_t* out, uint16_t* h_routed, uint16_t* h_shared) {
+                      const uint8_t* qs_dn, const uint16_t* ss_dn, const uint16_t* residual,
+                      const int64_t* tokens, int64_t n_tokens, uint16_t* out, uint16_t* h_routed,
+                      uint16_t* h_shared) {
     int64_t gu_bytes = (int64_t)2 * F * (d / 2), gu_scales = (int64_t)2 * F * (d / group);
     int64_t dn_bytes = (int64_t)d * (F / 2), dn_scales = (int64_t)d * (F / group);
     float* y = (float*)malloc(sizeof(float) * (size_t)d);
@@ -324,6 +329,7 @@ void orc_layer_tokens(const uint16_t* x, int32_t d, int32_t E, int32_t k, int32_
         if (h_shared) memcpy(h_shared + n * Fs, h, sizeof(uint16_t) * (size_t)Fs);
         for (int32_t c = 0; c < d; ++c) {
             acc[c] = acc[c] + y[c];
+            if (residual) acc[c] = orc_bf16_to_f32(residual[t * d + c]) + acc[c];
             out[n * d + c] = orc_f32_to_bf16(acc[c]);
         }
     }

@@ -58,14 +58,16 @@ void orc_expert_token(const uint16_t* x, int32_t d, int32_t F, int32_t group,
 /* Layer output for the listed tokens: out[n][d] bf16 for token tokens[n].
    Routed weights are stacked over experts: q_gu [E][2F][d/2], s_gu
    [E][2F][d/group], q_dn [E][d][F/2], s_dn [E][d][F/group]; the shared expert
-   has F = Fs.  h_routed (nullable) receives [n][k][F], h_shared (nullable)
-   [n][Fs]. */
+   has F = Fs.  residual (nullable) is a bf16 [T][d] row per token, added in
+   fp32 after the routed + shared sum and before the one bf16 rounding.
+   h_routed (nullable) receives [n][k][F], h_shared (nullable) [n][Fs]. */
 void orc_layer_tokens(const uint16_t* x, int32_t d, int32_t E, int32_t k, int32_t F, int32_t Fs,
                       int32_t group, const int32_t* topk_idx, const float* topk_w,
                       const uint8_t* q_gu, const uint16_t* s_gu, const uint8_t* q_dn,
                       const uint16_t* s_dn, const uint8_t* qs_gu, const uint16_t* ss_gu,
-                      const uint8_t* qs_dn, const uint16_t* ss_dn, const int64_t* tokens,
-                      int64_t n_tokens, uint16_t* out, uint16_t* h_routed, uint16_t* h_shared);
+                      const uint8_t* qs_dn, const uint16_t* ss_dn, const uint16_t* residual,
+                      const int64_t* tokens, int64_t n_tokens, uint16_t* out, uint16_t* h_routed,
+                      uint16_t* h_shared);
 
 /* Element-wise array forms of the format conversions. */
 void orc_f32_to_f16_array(const float* x, int64_t n, uint16_t* out);

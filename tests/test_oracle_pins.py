@@ -475,3 +475,70 @@ def test_layer_down_scale_power_of_two(oracle_lib):
     o1 = _x_f64(res["out"])
     o2 = _x_f64(res2["out"])
     assert np.array_equal(o2, 2 * o1)
+
+
+# ------------------------------------------------------------------ residual add (add3)
+
+
+def _bf16_bits(v):
+    return torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def test_residual_negative_zero_is_identity(oracle_lib):
+    """-0 is the additive identity of IEEE addition (x + -0 == x bit for bit,
+    -0 included), so a residual of -0 leaves every output bit unchanged."""
+    xb, Wr, b, Wgu, Wd, Wgu_s, Wd_s = _random_layer(oracle_lib, seed=10)
+    W = _pack_expert_stack(oracle_lib, Wgu, Wd, Wgu_s, Wd_s, 16)
+    plain = oracle_lib.layer(xb, Wr, b, W, 3)["out"]
+    neg0 = np.full(xb.shape, 0x8000, np.uint16)
+    assert np.array_equal(oracle_lib.layer(xb, Wr, b, W, 3, residual=neg0)["out"], plain)
+
+
+def test_residual_with_zero_experts_is_the_residual(oracle_lib):
+    """All expert weights zero: the routed + shared sum is +0, and r + 0 = r is
+    already a bf16 value, so the output is the residual itself."""
+    xb, Wr, b, Wgu, Wd, Wgu_s, Wd_s = _random_layer(oracle_lib, seed=11)
+    W = _pack_expert_stack(oracle_lib, 0 * Wgu, 0 * Wd, 0 * Wgu_s, 0 * Wd_s, 16)
+    r = _bf16_bits(np.random.default_rng(12).standard_normal(xb.shape) * 3)
+    assert np.array_equal(oracle_lib.layer(xb, Wr, b, W, 3, residual=r)["out"], r)
+
+
+def test_residual_added_after_routed_plus_shared(oracle_lib):
+    """out = bf16(r + (routed + shared)) with the bracket summed first, against the
+    dense-masked route.  Residuals are chosen per element, where one exists, so that
+    the other grouping, (r + routed) + shared, would round to a different bf16
+    value: a kernel or oracle that adds in the wrong order fails there."""
+    d, E, k, F, Fs, group = 64, 8, 3, 32, 32, 16
+    xb, Wr, b, Wgu, Wd, Wgu_s, Wd_s = _random_layer(oracle_lib, seed=13, d=d, E=E, k=k, F=F,
+                                                     Fs=Fs, group=group)
+    W = _pack_expert_stack(oracle_lib, Wgu, Wd, Wgu_s, Wd_s, group)
+    sel = oracle_lib.layer(xb, Wr, b, W, k)
+    T = xb.shape[0]
+    routed = np.zeros((T, d), np.float32)
+    shared = np.zeros((T, d), np.float32)
+    for t in range(T):
+        for j in range(k):
+            e = sel["topk_idx"][t, j]
+            _, y = oracle_lib.expert_token(xb[t], W.q_gu[e], W.s_gu[e], W.q_dn[e], W.s_dn[e],
+                                           group)
+            routed[t] = routed[t] + sel["topk_w"][t, j] * y
+        _, shared[t] = oracle_lib.expert_token(xb[t], W.qs_gu, W.ss_gu, W.qs_dn, W.ss_dn, group)
+    # candidate residuals: every bf16 value with 2^-6 <= |r| < 2^8
+    cand = (np.arange(1 << 16, dtype=np.uint32) << 16).view(np.float32)
+    cand = cand[np.isfinite(cand) & (np.abs(cand) >= 2.0 ** -6) & (np.abs(cand) < 2.0 ** 8)]
+    r = np.full((T, d), 1.0, np.float32)
+    separating = np.zeros((T, d), bool)
+    for t in range(T):
+        for c in range(d):
+            first = _bf16_bits(cand + (routed[t, c] + shared[t, c]))
+            other = _bf16_bits((cand + routed[t, c]) + shared[t, c])
+            hit = np.nonzero(first != other)[0]
+            if hit.size:
+                r[t, c] = cand[hit[0]]
+                separating[t, c] = True
+    assert separating.sum() >= 1
+    rb = _bf16_bits(r)
+    out = oracle_lib.layer(xb, Wr, b, W, k, residual=rb)["out"]
+    assert np.array_equal(out, _bf16_bits(r + (routed + shared)))
+    assert not np.array_equal(out[separating], _bf16_bits((r + routed) + shared)[separating])
