@@ -113,6 +113,12 @@ const char* moe_status_string(moe_status_t status);
 moe_status_t moe_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group, uint8_t* q,
                          uint16_t* s, void* stream);
 
+/* moe_pack_w4_bytes -- sizes of moe_pack_w4's outputs for these arguments:
+ * returns the packed bytes (rows * K/2) and writes the scale bytes
+ * (rows * K/group * 2) to *scale_bytes when that is non-null.  Host only, no
+ * CUDA call.  Returns 0 (and writes 0) for arguments moe_pack_w4 rejects. */
+size_t moe_pack_w4_bytes(int64_t rows, int64_t K, int32_t group, size_t* scale_bytes);
+
 /* Bytes of workspace the per-step calls below need for these dimensions
    (the same number serves every call; 0 on invalid dims). */
 size_t moe_workspace_bytes(const moe_dims_t* dims);
@@ -242,6 +248,22 @@ moe_status_t moe_down_w4a16(const uint16_t* H, const moe_dims_t* dims, const int
 moe_status_t moe_combine_shared(const float* Y, const float* topk_w, const int32_t* pos,
                                 const moe_dims_t* dims, uint16_t* out, void* stream);
 
+/* moe_combine_shared_residual -- moe_combine_shared plus a residual row in
+ * the same launch (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
+ * residual + routed accumulator + shared output in one kernel, the routed and
+ * shared terms summed first):
+ *   out[t] = bf16( float(residual[t]) + (sum_j topk_w[t][j] * Y[pos[t*k+j]]
+ *                                        + Y[T*k + t]) ),
+ * the bracket summed in fp32 in the order of moe_combine_shared, one rounding.
+ *   residual (device) bf16 [T][d], 16-byte aligned; may be the same buffer
+ *            as out (in-place residual update)
+ *   out      (device) out: bf16 [T][d], 16-byte aligned
+ * MOE_ERR_INVALID_ARG for a null or misaligned residual or out.
+ */
+moe_status_t moe_combine_shared_residual(const float* Y, const float* topk_w, const int32_t* pos,
+                                         const moe_dims_t* dims, const uint16_t* residual,
+                                         uint16_t* out, void* stream);
+
 /* ----------------------------------------------------------------------------
  * moe_layer_forward -- the whole layer in one call: router, descriptors,
  * gate+up SwiGLU, down, combine, with the intermediates in the workspace.
@@ -259,6 +281,17 @@ moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float*
                                const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd,
                                moe_w4_t Wgu_s, moe_w4_t Wd_s, uint16_t* out, void* ws,
                                size_t ws_bytes, void* stream);
+
+/* moe_layer_forward_residual -- moe_layer_forward with the residual add of
+ * moe_combine_shared_residual folded into the layer's last kernel (the
+ * combine, or on the GEMV path the down kernel's fused combine): out =
+ * bf16(residual + (routed + shared)).  residual and out are bf16 [T][d],
+ * 16-byte aligned; out may be the residual buffer (in-place update), not x.
+ * Same workspace and launches as moe_layer_forward. */
+moe_status_t moe_layer_forward_residual(const uint16_t* x, const float* W_r, const float* bias,
+                                        const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd,
+                                        moe_w4_t Wgu_s, moe_w4_t Wd_s, const uint16_t* residual,
+                                        uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_layer_forward_host -- as moe_layer_forward, but x_host is read from
  * host memory and the output is written to out_host: the call enqueues the

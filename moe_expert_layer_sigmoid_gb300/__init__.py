@@ -35,7 +35,8 @@ EXPORTS = (
     "moe_status_string", "moe_pack_w4", "moe_workspace_bytes", "moe_router_topk",
     "moe_build_descriptors", "moe_gateup_swiglu_w4a16", "moe_down_w4a16", "moe_combine_shared",
     "moe_layer_workspace_bytes", "moe_layer_forward", "moe_layer_forward_host",
-    "moe_check_device_status", "moe_router_topk_noalloc",
+    "moe_check_device_status", "moe_router_topk_noalloc", "moe_pack_w4_bytes",
+    "moe_combine_shared_residual", "moe_layer_forward_residual",
 )
 
 
@@ -84,7 +85,10 @@ def lib() -> ctypes.CDLL:
         "moe_build_descriptors": ([p, D, p, p, p, p, p, p, sz, p], i32),
         "moe_gateup_swiglu_w4a16": ([p, D, p, p, p, W4, W4, p, p, sz, p], i32),
         "moe_down_w4a16": ([p, D, p, p, W4, W4, p, p, sz, p], i32),
+        "moe_pack_w4_bytes": ([i64, i64, i32, ctypes.POINTER(sz)], sz),
         "moe_combine_shared": ([p, p, p, D, p, p], i32),
+        "moe_combine_shared_residual": ([p, p, p, D, p, p, p], i32),
+        "moe_layer_forward_residual": ([p, p, p, D, W4, W4, W4, W4, p, p, p, sz, p], i32),
         "moe_layer_forward": ([p, p, p, D, W4, W4, W4, W4, p, p, sz, p], i32),
         "moe_layer_forward_host": ([p, p, p, D, W4, W4, W4, W4, p, p, sz, p], i32),
         "moe_check_device_status": ([p, sz, p], i32),
@@ -216,6 +220,32 @@ def moe_combine_shared(Y, topk_w, pos, dims: Dims, out, stream=None):
         _dev(Y, torch.float32, "Y"), _dev(topk_w, torch.float32, "topk_w"),
         _dev(pos, torch.int32, "pos"), ctypes.byref(dims), _dev(out, torch.int16, "out"),
         _stream(stream)), "moe_combine_shared")
+
+
+def moe_combine_shared_residual(Y, topk_w, pos, dims: Dims, residual, out, stream=None):
+    """out = bf16(residual + (routed + shared)); out may be residual itself."""
+    _check(lib().moe_combine_shared_residual(
+        _dev(Y, torch.float32, "Y"), _dev(topk_w, torch.float32, "topk_w"),
+        _dev(pos, torch.int32, "pos"), ctypes.byref(dims), _dev(residual, torch.int16, "residual"),
+        _dev(out, torch.int16, "out"), _stream(stream)), "moe_combine_shared_residual")
+
+
+def moe_layer_forward_residual(x, W_r, bias, dims: Dims, Wgu: W4, Wd: W4, Wgu_s: W4, Wd_s: W4,
+                               residual, out, ws, stream=None):
+    """The layer with the residual add in its last kernel; out may be residual itself."""
+    _check(lib().moe_layer_forward_residual(
+        _dev(x, torch.int16, "x"), _dev(W_r, torch.float32, "W_r"),
+        _dev(bias, torch.float32, "bias"), ctypes.byref(dims), Wgu, Wd, Wgu_s, Wd_s,
+        _dev(residual, torch.int16, "residual"), _dev(out, torch.int16, "out"), _ptr(ws),
+        ws.numel(), _stream(stream)), "moe_layer_forward_residual")
+
+
+def moe_pack_w4_bytes(rows: int, K: int, group: int) -> tuple[int, int]:
+    """(packed bytes, scale bytes) of moe_pack_w4's output; (0, 0) for arguments it
+    rejects."""
+    sb = ctypes.c_size_t(0)
+    qb = lib().moe_pack_w4_bytes(rows, K, group, ctypes.byref(sb))
+    return int(qb), int(sb.value)
 
 
 def moe_layer_forward(x, W_r, bias, dims: Dims, Wgu: W4, Wd: W4, Wgu_s: W4, Wd_s: W4, out, ws,

@@ -133,6 +133,10 @@ moe_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
     return MOE_OK;
 }
 
+// A bf16 activation row buffer read or written in 8-byte pieces; 16-byte
+// alignment (what any device allocation gives) is required.
+bool act_ok(const void* p) { return p && reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
 // q is read with 16-byte loads, s with 2-byte loads.
 bool w4_ok(moe_w4_t w) {
     return w.q && w.s && reinterpret_cast<uintptr_t>(w.q) % 16 == 0 &&
@@ -182,12 +186,74 @@ moe_status_t down_impl(const uint16_t* H, const moe_dims_t& d, const int32_t* of
     switch (expert_path(d)) {
         case Path::kGemv:
             return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, nullptr, nullptr,
-                                            nullptr, nullptr, hdr, false, st));
+                                            nullptr, nullptr, nullptr, hdr, false, st));
         case Path::kGrouped:
             return map_err(launch_down_grouped(H, d, Wd, Wd_s, Y, hdr,
                                                ws_at<int4>(ws, L.tiles) + L.max_tiles, st));
         default: return MOE_ERR_UNSUPPORTED;
     }
+}
+
+// The whole layer; `residual` null for the plain output.
+moe_status_t layer_forward(const uint16_t* x, const float* W_r, const float* bias,
+                           const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd, moe_w4_t Wgu_s,
+                           moe_w4_t Wd_s, const uint16_t* residual, uint16_t* out, void* ws,
+                           size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.layer_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!x || !W_r || !bias || !out || !w4_ok(Wgu) || !w4_ok(Wd) || !w4_ok(Wgu_s) || !w4_ok(Wd_s))
+        return MOE_ERR_INVALID_ARG;
+    const moe_dims_t& d = *dims;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* topk_idx = ws_at<int32_t>(ws, L.topk_idx);
+    float* topk_w = ws_at<float>(ws, L.topk_w);
+    int32_t* counts = ws_at<int32_t>(ws, L.counts);
+    int32_t* offsets = ws_at<int32_t>(ws, L.offsets);
+    int32_t* perm = ws_at<int32_t>(ws, L.perm);
+    int32_t* pos = ws_at<int32_t>(ws, L.pos);
+    int32_t* sched = ws_at<int32_t>(ws, L.sched);
+    uint16_t* H = ws_at<uint16_t>(ws, L.H);
+    float* Y = ws_at<float>(ws, L.Y);
+    WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
+    const Path path = expert_path(d);
+    if (path == Path::kUnsupported) return MOE_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (path == Path::kGemv) {
+        // decode chain: fused router + descriptors, then the two GEMVs with the
+        // combine fused into the down kernel; each waits on its predecessor
+        // through programmatic dependent launch
+        if (d.T <= kMaxDecodeT) {
+            e = launch_router_decode(x, W_r, bias, d, topk_idx, topk_w, nullptr,
+                                     ws_at<float>(ws, L.logits), L.router_ksplit, counts, offsets,
+                                     perm, pos, sched, hdr, s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+        } else {
+            e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
+                              ws_at<float>(ws, L.logits), L.router_ksplit, L.router_ksplit_large, s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
+                                   ws_at<int4>(ws, L.tiles), L.max_tiles,
+                                   ws_at<int32_t>(ws, L.hist), s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+        }
+        e = launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, &hdr->n_active, hdr,
+                               true, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, &hdr->n_active, topk_w,
+                                        pos, residual, out, hdr, true, s));
+    }
+    e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr, ws_at<float>(ws, L.logits),
+                      L.router_ksplit, L.router_ksplit_large, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
+                           ws_at<int4>(ws, L.tiles), L.max_tiles, ws_at<int32_t>(ws, L.hist), s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if ((st = gateup_impl(x, d, offsets, perm, sched, Wgu, Wgu_s, H, ws, s)) != MOE_OK) return st;
+    if ((st = down_impl(H, d, offsets, sched, Wd, Wd_s, Y, ws, s)) != MOE_OK) return st;
+    return map_err(launch_combine(Y, topk_w, pos, d, residual, out, s));
 }
 
 }  // namespace
@@ -204,6 +270,14 @@ const char* moe_status_string(moe_status_t s) {
         case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK: a device-side check tripped";
     }
     return "unknown moe_status_t";
+}
+
+size_t moe_pack_w4_bytes(int64_t rows, int64_t K, int32_t group, size_t* scale_bytes) {
+    if (scale_bytes) *scale_bytes = 0;
+    if (rows < 0 || K <= 0 || group <= 0 || K % group) return 0;
+    if (!(group == 8 || group == 16 || group_ok(group))) return 0;
+    if (scale_bytes) *scale_bytes = (size_t)rows * (size_t)(K / group) * sizeof(uint16_t);
+    return (size_t)rows * (size_t)(K / 2);
 }
 
 moe_status_t moe_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group, uint8_t* q,
@@ -291,68 +365,36 @@ moe_status_t moe_combine_shared(const float* Y, const float* topk_w, const int32
     if (st != MOE_OK) return st;
     if (dims->T == 0) return MOE_OK;
     if (!Y || !topk_w || !pos || !out) return MOE_ERR_INVALID_ARG;
-    return map_err(launch_combine(Y, topk_w, pos, *dims, out, static_cast<cudaStream_t>(stream)));
+    return map_err(launch_combine(Y, topk_w, pos, *dims, nullptr, out,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_combine_shared_residual(const float* Y, const float* topk_w, const int32_t* pos,
+                                         const moe_dims_t* dims, const uint16_t* residual,
+                                         uint16_t* out, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!Y || !topk_w || !pos || !act_ok(residual) || !act_ok(out)) return MOE_ERR_INVALID_ARG;
+    return map_err(launch_combine(Y, topk_w, pos, *dims, residual, out,
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_layer_forward(const uint16_t* x, const float* W_r, const float* bias,
                                const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd,
                                moe_w4_t Wgu_s, moe_w4_t Wd_s, uint16_t* out, void* ws,
                                size_t ws_bytes, void* stream) {
-    moe_status_t st = check_dims(dims);
-    if (st != MOE_OK) return st;
-    const WsLayout L = ws_layout(*dims);
-    if ((st = check_ws(ws, ws_bytes, L.layer_bytes)) != MOE_OK) return st;
-    if (dims->T == 0) return MOE_OK;
-    if (!x || !W_r || !bias || !out || !w4_ok(Wgu) || !w4_ok(Wd) || !w4_ok(Wgu_s) || !w4_ok(Wd_s))
-        return MOE_ERR_INVALID_ARG;
-    const moe_dims_t& d = *dims;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int32_t* topk_idx = ws_at<int32_t>(ws, L.topk_idx);
-    float* topk_w = ws_at<float>(ws, L.topk_w);
-    int32_t* counts = ws_at<int32_t>(ws, L.counts);
-    int32_t* offsets = ws_at<int32_t>(ws, L.offsets);
-    int32_t* perm = ws_at<int32_t>(ws, L.perm);
-    int32_t* pos = ws_at<int32_t>(ws, L.pos);
-    int32_t* sched = ws_at<int32_t>(ws, L.sched);
-    uint16_t* H = ws_at<uint16_t>(ws, L.H);
-    float* Y = ws_at<float>(ws, L.Y);
-    WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
-    const Path path = expert_path(d);
-    if (path == Path::kUnsupported) return MOE_ERR_UNSUPPORTED;
-    cudaError_t e;
-    if (path == Path::kGemv) {
-        // decode chain: fused router + descriptors, then the two GEMVs with the
-        // combine fused into the down kernel; each waits on its predecessor
-        // through programmatic dependent launch
-        if (d.T <= kMaxDecodeT) {
-            e = launch_router_decode(x, W_r, bias, d, topk_idx, topk_w, nullptr,
-                                     ws_at<float>(ws, L.logits), L.router_ksplit, counts, offsets,
-                                     perm, pos, sched, hdr, s);
-            if (e != cudaSuccess) return MOE_ERR_CUDA;
-        } else {
-            e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
-                              ws_at<float>(ws, L.logits), L.router_ksplit, L.router_ksplit_large, s);
-            if (e != cudaSuccess) return MOE_ERR_CUDA;
-            e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
-                                   ws_at<int4>(ws, L.tiles), L.max_tiles,
-                                   ws_at<int32_t>(ws, L.hist), s);
-            if (e != cudaSuccess) return MOE_ERR_CUDA;
-        }
-        e = launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, &hdr->n_active, hdr,
-                               true, s);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-        return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, &hdr->n_active, topk_w,
-                                        pos, out, hdr, true, s));
-    }
-    e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr, ws_at<float>(ws, L.logits),
-                      L.router_ksplit, L.router_ksplit_large, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
-                           ws_at<int4>(ws, L.tiles), L.max_tiles, ws_at<int32_t>(ws, L.hist), s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if ((st = gateup_impl(x, d, offsets, perm, sched, Wgu, Wgu_s, H, ws, s)) != MOE_OK) return st;
-    if ((st = down_impl(H, d, offsets, sched, Wd, Wd_s, Y, ws, s)) != MOE_OK) return st;
-    return map_err(launch_combine(Y, topk_w, pos, d, out, s));
+    return layer_forward(x, W_r, bias, dims, Wgu, Wd, Wgu_s, Wd_s, nullptr, out, ws, ws_bytes,
+                         stream);
+}
+
+moe_status_t moe_layer_forward_residual(const uint16_t* x, const float* W_r, const float* bias,
+                                        const moe_dims_t* dims, moe_w4_t Wgu, moe_w4_t Wd,
+                                        moe_w4_t Wgu_s, moe_w4_t Wd_s, const uint16_t* residual,
+                                        uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+    if (dims && dims->T > 0 && (!act_ok(residual) || !act_ok(out))) return MOE_ERR_INVALID_ARG;
+    return layer_forward(x, W_r, bias, dims, Wgu, Wd, Wgu_s, Wd_s, residual, out, ws, ws_bytes,
+                         stream);
 }
 
 moe_status_t moe_layer_forward_host(const uint16_t* x_host, const float* W_r, const float* bias,

@@ -103,7 +103,8 @@ cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int
 // null, in which case the kernels count them from offsets and sched.  `pdl`
 // launches with programmatic stream serialisation: the kernel's prologue
 // overlaps the previous kernel, and it waits for it before reading its
-// outputs.  With `out` non-null the down kernel also does the combine.
+// outputs.  With `out` non-null the down kernel also does the combine (plus
+// `residual` when that is non-null; `out` may alias it).
 bool gemv_supported(const moe_dims_t& d);
 cudaError_t launch_gateup_gemv(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,
                                const int32_t* perm, const int32_t* sched, moe_w4_t Wgu,
@@ -113,7 +114,8 @@ cudaError_t launch_gateup_gemv(const uint16_t* x, const moe_dims_t& d, const int
 cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32_t* offsets,
                              const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y,
                              const int32_t* n_active, const float* topk_w, const int32_t* pos,
-                             uint16_t* out, WsHeader* hdr, bool pdl, cudaStream_t st);
+                             const uint16_t* residual, uint16_t* out, WsHeader* hdr, bool pdl,
+                             cudaStream_t st);
 
 // Fused decode router: logits, top-k and descriptors in one launch (T <= 64).
 cudaError_t launch_router_decode(const uint16_t* x, const float* W_r, const float* bias,
@@ -134,8 +136,11 @@ cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t
                                 moe_w4_t Wd_s, float* Y, WsHeader* hdr, const int4* tiles,
                                 cudaStream_t st);
 
+// `residual` (nullable, bf16 [T][d]) is added to the routed + shared sum
+// before the bf16 rounding; `out` may alias it.
 cudaError_t launch_combine(const float* Y, const float* topk_w, const int32_t* pos,
-                           const moe_dims_t& d, uint16_t* out, cudaStream_t st);
+                           const moe_dims_t& d, const uint16_t* residual, uint16_t* out,
+                           cudaStream_t st);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();

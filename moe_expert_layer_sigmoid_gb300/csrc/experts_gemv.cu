@@ -493,6 +493,7 @@ struct DnArgs {
     const int32_t* n_active;
     const float* topk_w;  // fused combine when out is non-null
     const int32_t* pos;
+    const uint16_t* residual;  // added after routed + shared when non-null; may alias out
     uint16_t* out;
     WsHeader* hdr;
 };
@@ -630,6 +631,13 @@ __device__ __forceinline__ void dn_combine(const DnArgs& a, int q_lo, int nqc) {
         acc.y += ys.y;
         acc.z += ys.z;
         acc.w += ys.w;
+        if (a.residual) {
+            const uint2 r = *reinterpret_cast<const uint2*>(a.residual + (int64_t)t * d + c);
+            acc.x = bf16_lo(r.x) + acc.x;
+            acc.y = bf16_hi(r.x) + acc.y;
+            acc.z = bf16_lo(r.y) + acc.z;
+            acc.w = bf16_hi(r.y) + acc.w;
+        }
         uint2 o;
         o.x = (uint32_t)float_to_bf16_bits(acc.x) | ((uint32_t)float_to_bf16_bits(acc.y) << 16);
         o.y = (uint32_t)float_to_bf16_bits(acc.z) | ((uint32_t)float_to_bf16_bits(acc.w) << 16);
@@ -795,7 +803,8 @@ cudaError_t launch_gateup_gemv(const uint16_t* x, const moe_dims_t& d, const int
 cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32_t* offsets,
                              const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y,
                              const int32_t* n_active, const float* topk_w, const int32_t* pos,
-                             uint16_t* out, WsHeader* hdr, bool pdl, cudaStream_t st) {
+                             const uint16_t* residual, uint16_t* out, WsHeader* hdr, bool pdl,
+                             cudaStream_t st) {
     DnArgs a;
     a.H = H;
     a.ldh = std::max(d.F, d.F_s);
@@ -816,6 +825,7 @@ cudaError_t launch_down_gemv(const uint16_t* H, const moe_dims_t& d, const int32
     a.n_active = n_active;
     a.topk_w = topk_w;
     a.pos = pos;
+    a.residual = residual;
     a.out = out;
     a.hdr = hdr;
     if (!gemv_supported(d)) return cudaErrorInvalidValue;

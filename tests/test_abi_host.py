@@ -118,3 +118,36 @@ def test_zero_tokens_validates_then_returns_ok(L):
     bad = _dims(T=0, group=48)
     assert L.moe_layer_forward(None, None, None, ctypes.byref(bad), moe.W4(), moe.W4(), moe.W4(),
                                moe.W4(), None, ws, need, None) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_pack_w4_bytes(L):
+    assert moe.moe_pack_w4_bytes(6, 256, 32) == (6 * 128, 6 * 8 * 2)
+    assert moe.moe_pack_w4_bytes(0, 128, 128) == (0, 0)
+    assert moe.moe_pack_w4_bytes(4, 100, 32) == (0, 0)   # K % group != 0
+    assert moe.moe_pack_w4_bytes(4, 96, 48) == (0, 0)    # unsupported group
+    assert moe.moe_pack_w4_bytes(-1, 128, 32) == (0, 0)
+    big = moe.moe_pack_w4_bytes(256 * 2048, 4096, 128)  # every routed gate+up row of a layer
+    assert big == (256 * 2048 * 2048, 256 * 2048 * 32 * 2)
+
+
+def test_residual_calls_validate_before_launch(L):
+    d = _dims()
+    need = moe.moe_layer_workspace_bytes(d)
+    ws = 1 << 20  # never dereferenced: validation fails first
+    assert L.moe_layer_forward_residual(None, None, None, ctypes.byref(d), moe.W4(), moe.W4(),
+                                        moe.W4(), moe.W4(), None, None, ws, need,
+                                        None) == moe.MOE_ERR_INVALID_ARG
+    # misaligned residual or out
+    assert L.moe_layer_forward_residual(None, None, None, ctypes.byref(d), moe.W4(), moe.W4(),
+                                        moe.W4(), moe.W4(), 4096 + 8, 8192, ws, need,
+                                        None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_shared_residual(4096, 4096, 4096, ctypes.byref(d), 4096 + 2, 8192,
+                                         None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_shared_residual(None, None, None, ctypes.byref(_dims(group=48)), None,
+                                         None, None) == moe.MOE_ERR_UNSUPPORTED
+    d0 = _dims(T=0)
+    assert L.moe_layer_forward_residual(None, None, None, ctypes.byref(d0), moe.W4(), moe.W4(),
+                                        moe.W4(), moe.W4(), None, None, ws,
+                                        moe.moe_layer_workspace_bytes(d0), None) == moe.MOE_OK
+    assert L.moe_combine_shared_residual(None, None, None, ctypes.byref(d0), None, None,
+                                         None) == moe.MOE_OK
