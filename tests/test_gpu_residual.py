@@ -89,12 +89,12 @@ def test_negative_zero_residual_and_in_place_are_exact(C, flags):
 
 
 def test_combine_residual_bit_exact_on_exact_products():
-    """Weights 1/4 and bf16 rows make every product exact, so the kernel's fused
-    multiply-adds equal plain fp32 adds in the stated order."""
+    """Weights 1/4 (a power of two) make every product exact, so the kernel's fused
+    multiply-adds equal plain fp32 adds in the stated order; the rows are full fp32
+    values, so the sums round and the grouping shows."""
     T, d, k, E = 6, 512, 4, 16
     rng = np.random.default_rng(90)
-    Y = _bf16_bits(rng.standard_normal((T * k + T, d)))
-    Yf = (Y.astype(np.uint32) << 16).view(np.float32)
+    Yf = rng.standard_normal((T * k + T, d)).astype(np.float32)
     topk_w = np.full((T, k), 0.25, np.float32)
     pos = rng.permutation(T * k).astype(np.int32)
     routed = np.zeros((T, d), np.float32)
