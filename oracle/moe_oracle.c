@@ -46,10 +46,10 @@
  *  R8 descriptors: perm lists slot ids t*k + j sorted by (expert, token);
  *     pos is its inverse; sched orders experts by count, largest first, ties
  *     to the lower id.
- *  R9 residual add (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
- *     residual + routed + shared in one launch, routed and shared summed
- *     first): with a residual row r (bf16), out = bf16(float(r) + acc), where
- *     acc is the fp32 routed + shared sum of R5, rounded once.
+ *  R10 residual add (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
+ *      residual + routed + shared in one launch, routed and shared summed
+ *      first): with a residual row r (bf16), out = bf16(float(r) + acc), where
+ *      acc is the fp32 routed + shared sum of R5, rounded once.
  */
 #include "moe_oracle.h"
 
