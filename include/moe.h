@@ -20,6 +20,11 @@
  *    no host read of device data, so a sequence of calls can be captured into
  *    a CUDA graph.  moe_check_device_status is the one exception (it syncs).
  *  - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
+ *  - Alignment: x, W_r, H, Y, out and residual must be 16-byte aligned (they
+ *    are accessed with vector loads and stores; any device allocation is),
+ *    packed weights q 16-byte and scales 2-byte aligned, the workspace
+ *    256-byte aligned.  A misaligned pointer is MOE_ERR_INVALID_ARG (the
+ *    workspace: MOE_ERR_WORKSPACE), never a device fault.
  *  - Argument errors are detected on the host before anything is launched and
  *    returned synchronously; nothing is enqueued in that case.  A failed
  *    launch returns MOE_ERR_CUDA.  Device-side consistency checks (an expert

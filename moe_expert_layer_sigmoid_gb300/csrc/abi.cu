@@ -64,11 +64,14 @@ WsLayout ws_layout(const moe_dims_t& d) {
 }
 
 int sm_count() {
-    static int counts[64] = {};
+    // cached per device; host threads may race to fill an entry with the same value
+    static std::atomic<int> counts[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!counts[dev]) cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev);
-    return counts[dev];
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (!n && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        counts[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
@@ -96,17 +99,10 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
     return cudaSuccess;
 }
 
-}  // namespace moe
-
-using namespace moe;
-
-namespace {
-
-moe_status_t map_err(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
-
+// Quantisation groups the layer kernels take.
 bool group_ok(int g) { return g == 32 || g == 64 || g == 128; }
 
-// Shape validation shared by the per-step calls.
+// Shape validation shared by every entry point that takes moe_dims_t.
 moe_status_t check_dims(const moe_dims_t* d) {
     if (!d) return MOE_ERR_INVALID_ARG;
     if (d->T < 0 || d->d <= 0 || d->E <= 0 || d->k <= 0 || d->F <= 0 || d->F_s <= 0 ||
@@ -127,15 +123,24 @@ moe_status_t check_dims(const moe_dims_t* d) {
     return MOE_OK;
 }
 
+// Activation and fp32 buffers are read or written with vector accesses of up
+// to 16 bytes; 16-byte alignment (what any device allocation gives) is
+// required, so a misaligned pointer is an argument error, never a fault.
+bool act_ok(const void* p) { return p && reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+moe_status_t map_err(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
 moe_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
     if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(ws) % 256) return MOE_ERR_WORKSPACE;
     return MOE_OK;
 }
-
-// A bf16 activation row buffer read or written in 8-byte pieces; 16-byte
-// alignment (what any device allocation gives) is required.
-bool act_ok(const void* p) { return p && reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
 // q is read with 16-byte loads, s with 2-byte loads.
 bool w4_ok(moe_w4_t w) {
@@ -204,7 +209,8 @@ moe_status_t layer_forward(const uint16_t* x, const float* W_r, const float* bia
     const WsLayout L = ws_layout(*dims);
     if ((st = check_ws(ws, ws_bytes, L.layer_bytes)) != MOE_OK) return st;
     if (dims->T == 0) return MOE_OK;
-    if (!x || !W_r || !bias || !out || !w4_ok(Wgu) || !w4_ok(Wd) || !w4_ok(Wgu_s) || !w4_ok(Wd_s))
+    if (!act_ok(x) || !act_ok(W_r) || !bias || !act_ok(out) || !w4_ok(Wgu) || !w4_ok(Wd) ||
+        !w4_ok(Wgu_s) || !w4_ok(Wd_s))
         return MOE_ERR_INVALID_ARG;
     const moe_dims_t& d = *dims;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -311,7 +317,7 @@ moe_status_t moe_router_topk(const uint16_t* x, const float* W_r, const float* b
     const WsLayout L = ws_layout(*dims);
     if ((st = check_ws(ws, ws_bytes, L.step_bytes)) != MOE_OK) return st;
     if (dims->T == 0) return MOE_OK;
-    if (!x || !W_r || !bias || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!act_ok(x) || !act_ok(W_r) || !bias || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
     return map_err(launch_router(x, W_r, bias, *dims, topk_idx, topk_w, margin,
                                  ws_at<float>(ws, L.logits), L.router_ksplit,
                                  L.router_ksplit_large, static_cast<cudaStream_t>(stream)));
@@ -341,7 +347,7 @@ moe_status_t moe_gateup_swiglu_w4a16(const uint16_t* x, const moe_dims_t* dims,
     const WsLayout L = ws_layout(*dims);
     if ((st = check_ws(ws, ws_bytes, L.step_bytes)) != MOE_OK) return st;
     if (dims->T == 0) return MOE_OK;
-    if (!x || !offsets || !perm || !sched || !H || !w4_ok(Wgu) || !w4_ok(Wgu_s))
+    if (!act_ok(x) || !offsets || !perm || !sched || !act_ok(H) || !w4_ok(Wgu) || !w4_ok(Wgu_s))
         return MOE_ERR_INVALID_ARG;
     return gateup_impl(x, *dims, offsets, perm, sched, Wgu, Wgu_s, H, ws,
                        static_cast<cudaStream_t>(stream));
@@ -355,7 +361,8 @@ moe_status_t moe_down_w4a16(const uint16_t* H, const moe_dims_t* dims, const int
     const WsLayout L = ws_layout(*dims);
     if ((st = check_ws(ws, ws_bytes, L.step_bytes)) != MOE_OK) return st;
     if (dims->T == 0) return MOE_OK;
-    if (!H || !offsets || !sched || !Y || !w4_ok(Wd) || !w4_ok(Wd_s)) return MOE_ERR_INVALID_ARG;
+    if (!act_ok(H) || !offsets || !sched || !act_ok(Y) || !w4_ok(Wd) || !w4_ok(Wd_s))
+        return MOE_ERR_INVALID_ARG;
     return down_impl(H, *dims, offsets, sched, Wd, Wd_s, Y, ws, static_cast<cudaStream_t>(stream));
 }
 
@@ -364,7 +371,7 @@ moe_status_t moe_combine_shared(const float* Y, const float* topk_w, const int32
     moe_status_t st = check_dims(dims);
     if (st != MOE_OK) return st;
     if (dims->T == 0) return MOE_OK;
-    if (!Y || !topk_w || !pos || !out) return MOE_ERR_INVALID_ARG;
+    if (!act_ok(Y) || !topk_w || !pos || !act_ok(out)) return MOE_ERR_INVALID_ARG;
     return map_err(launch_combine(Y, topk_w, pos, *dims, nullptr, out,
                                   static_cast<cudaStream_t>(stream)));
 }
@@ -375,7 +382,8 @@ moe_status_t moe_combine_shared_residual(const float* Y, const float* topk_w, co
     moe_status_t st = check_dims(dims);
     if (st != MOE_OK) return st;
     if (dims->T == 0) return MOE_OK;
-    if (!Y || !topk_w || !pos || !act_ok(residual) || !act_ok(out)) return MOE_ERR_INVALID_ARG;
+    if (!act_ok(Y) || !topk_w || !pos || !act_ok(residual) || !act_ok(out))
+        return MOE_ERR_INVALID_ARG;
     return map_err(launch_combine(Y, topk_w, pos, *dims, residual, out,
                                   static_cast<cudaStream_t>(stream)));
 }

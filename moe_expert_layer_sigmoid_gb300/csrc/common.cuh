@@ -78,6 +78,10 @@ constexpr int kTileN = 128;
 
 WsLayout ws_layout(const moe_dims_t& d);
 
+// Host-side argument checks shared by the entry points (abi.cu).
+moe_status_t check_dims(const moe_dims_t* d);
+bool act_ok(const void* p);  // non-null and 16-byte aligned
+
 // ---------------------------------------------------------------------------
 // Launchers (defined in the .cu files).  All enqueue on `st` and return the
 // cudaGetLastError of the launch.

@@ -44,35 +44,21 @@ cudaError_t scratch_on_current_device(float** out) {
     return cudaSuccess;
 }
 
-// The same shape rules as the workspace form of the router.
-moe_status_t check_router_dims(const moe_dims_t* d) {
-    if (!d) return MOE_ERR_INVALID_ARG;
-    if (d->T < 0 || d->d <= 0 || d->E <= 0 || d->k <= 0 || d->F <= 0 || d->F_s <= 0 ||
-        d->group <= 0)
-        return MOE_ERR_INVALID_ARG;
-    if (d->k > d->E) return MOE_ERR_INVALID_ARG;
-    if ((int64_t)d->T * (d->k + 1) >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
-    if (!(d->group == 32 || d->group == 64 || d->group == 128)) return MOE_ERR_UNSUPPORTED;
-    if (d->d % 256 || d->F % 128 || d->F_s % 128) return MOE_ERR_UNSUPPORTED;
-    if (d->d % d->group || d->F % d->group || d->F_s % d->group) return MOE_ERR_UNSUPPORTED;
-    if (d->k > 32 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
-    return MOE_OK;
-}
-
 }  // namespace
 
 extern "C" moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* W_r,
                                                 const float* bias, const moe_dims_t* dims,
                                                 int32_t* topk_idx, float* topk_w, float* margin,
                                                 void* stream) {
-    moe_status_t st = check_router_dims(dims);
+    moe_status_t st = moe::check_dims(dims);
     if (st != MOE_OK) return st;
     const moe::WsLayout L = moe::ws_layout(*dims);
     const int ks = dims->T <= moe::kRouterSmallT ? L.router_ksplit : 1;
     const int64_t need = (int64_t)ks * dims->T * dims->E;
     if (need > (int64_t)kScratchFloats) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
     if (dims->T == 0) return MOE_OK;
-    if (!x || !W_r || !bias || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!moe::act_ok(x) || !moe::act_ok(W_r) || !bias || !topk_idx || !topk_w)
+        return MOE_ERR_INVALID_ARG;
     float* scratch = nullptr;
     if (scratch_on_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
     // The logits kernel writes every partial that the top-k kernel reads within

@@ -151,3 +151,30 @@ def test_residual_calls_validate_before_launch(L):
                                         moe.moe_layer_workspace_bytes(d0), None) == moe.MOE_OK
     assert L.moe_combine_shared_residual(None, None, None, ctypes.byref(d0), None, None,
                                          None) == moe.MOE_OK
+
+
+def test_misaligned_activation_pointers_rejected(L):
+    """x, W_r, H, Y and out are accessed with 16-byte vector loads and stores: a pointer
+    off a 16-byte boundary is an argument error before anything is enqueued."""
+    d = _dims()
+    step = moe.moe_workspace_bytes(d)
+    layer = moe.moe_layer_workspace_bytes(d)
+    ws = 1 << 20              # never dereferenced
+    ok, bad = 1 << 21, (1 << 21) + 8
+    INV = moe.MOE_ERR_INVALID_ARG
+    assert L.moe_router_topk(bad, ok, ok, ctypes.byref(d), ok, ok, None, ws, step, None) == INV
+    assert L.moe_router_topk(ok, bad, ok, ctypes.byref(d), ok, ok, None, ws, step, None) == INV
+    assert L.moe_router_topk_noalloc(bad, ok, ok, ctypes.byref(d), ok, ok, None, None) == INV
+    w4 = moe.W4(ok, ok)
+    assert L.moe_gateup_swiglu_w4a16(bad, ctypes.byref(d), ok, ok, ok, w4, w4, ok, ws, step,
+                                     None) == INV
+    assert L.moe_gateup_swiglu_w4a16(ok, ctypes.byref(d), ok, ok, ok, w4, w4, bad, ws, step,
+                                     None) == INV
+    assert L.moe_down_w4a16(bad, ctypes.byref(d), ok, ok, w4, w4, ok, ws, step, None) == INV
+    assert L.moe_down_w4a16(ok, ctypes.byref(d), ok, ok, w4, w4, bad, ws, step, None) == INV
+    assert L.moe_combine_shared(bad, ok, ok, ctypes.byref(d), ok, None) == INV
+    assert L.moe_combine_shared(ok, ok, ok, ctypes.byref(d), bad, None) == INV
+    assert L.moe_layer_forward(bad, ok, ok, ctypes.byref(d), w4, w4, w4, w4, ok, ws, layer,
+                               None) == INV
+    assert L.moe_layer_forward(ok, ok, ok, ctypes.byref(d), w4, w4, w4, w4, bad, ws, layer,
+                               None) == INV
