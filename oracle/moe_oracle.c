@@ -46,7 +46,7 @@
  *  R8 descriptors: perm lists slot ids t*k + j sorted by (expert, token);
  *     pos is its inverse; sched orders experts by count, largest first, ties
  *     to the lower id.
- *  R10 residual add (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
+ *  R14 residual add (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
  *      residual + routed + shared in one launch, routed and shared summed
  *      first): with a residual row r (bf16), out = bf16(float(r) + acc), where
  *      acc is the fp32 routed + shared sum of R5, rounded once.
