@@ -313,8 +313,11 @@ class GpuBench:
 
 # DRAM bytes (read + write) per step of the decode chain at decode1, summed over
 # router_decode_kernel, gateup_gemv_kernel and down_gemv_kernel from one
-# `ncu --set full` capture of each on this code (cold caches).
+# `ncu --set full` capture of each (cold caches).  down_gemv_kernel has changed
+# since (its combine takes an optional residual pointer), so the line reports
+# traffic as null and this figure as the prior capture until it is re-taken.
 DECODE1_TRAFFIC = 4_269_312 + 48_279_552 + 27_392 + 23_851_264
+DECODE1_TRAFFIC_CURRENT = False
 
 
 def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
@@ -333,7 +336,10 @@ def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
     return {"kernel": kernel,
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": DECODE1_TRAFFIC if cfg.name == "decode1" else None,
+            "traffic": (DECODE1_TRAFFIC if cfg.name == "decode1" and DECODE1_TRAFFIC_CURRENT
+                        else None),
+            **({"traffic_prior_capture": DECODE1_TRAFFIC}
+               if cfg.name == "decode1" and not DECODE1_TRAFFIC_CURRENT else {}),
             "bytes_per_step": int(nbytes),
             "router_weight_bytes_not_counted": router_bytes,
             "step_us": round(ms * 1e3, 3),
