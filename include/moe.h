@@ -48,6 +48,8 @@
  *    accumulate), H = bf16(silu(g) * u); Y = H . w^_down[c] (fp32 accumulate).
  *  - out[t] = bf16( sum_j w_tj * Y[pos(t, j)] + Y[shared row of t] ),
  *    accumulated in fp32 in the order j = 0..k-1, then the shared expert.
+ *    The _residual forms add a bf16 residual row r[t] to that finished fp32
+ *    sum before the one rounding: out[t] = bf16( r[t] + (routed + shared) ).
  *
  * Row numbering of the expert intermediates H [rows][F] and Y [rows][d]:
  * rows 0..T*k-1 are the routed slots in descriptor order (expert ascending,
@@ -66,7 +68,8 @@ extern "C" {
 
 typedef enum {
     MOE_OK = 0,
-    MOE_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size      */
+    MOE_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, negative or
+                                 inconsistent size                                */
     MOE_ERR_UNSUPPORTED = 2,  /* valid, but outside the shapes the kernels handle */
     MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required       */
     MOE_ERR_CUDA = 4,         /* a CUDA runtime call or a kernel launch failed    */
