@@ -54,6 +54,8 @@ def _get():
     sig = {
         "orc_pack_w4": [p, i64, i64, i32, p, p],
         "orc_dequant_w4": [p, p, i64, i64, i32, p],
+        "orc_dequant_q4_blocks": [p, i64, i64, p],
+        "orc_import_q4_blocks": [p, i64, i64, i32, p, p],
         "orc_router": [p, p, p, i64, i32, i32, i32, i64, i64, p, p, p, p],
         "orc_descriptors": [p, i64, i32, i32, p, p, p, p, p],
         "orc_expert_token": [p, i32, i32, i32, p, p, p, p, p, p],
@@ -144,6 +146,27 @@ def dequant_w4(q, s, group: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- router
+
+def dequant_q4_blocks(blocks, K: int) -> np.ndarray:
+    """GGUF-style Q4 blocks uint8 [rows][K/32*18] -> fp32 [rows][K]."""
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    rows = blocks.shape[0]
+    assert K % 32 == 0 and blocks.shape[1] == K // 32 * 18
+    w = np.empty((rows, K), np.float32)
+    _get().orc_dequant_q4_blocks(_p(blocks), rows, K, _p(w))
+    return w
+
+
+def import_q4_blocks(blocks, K: int, group: int):
+    """GGUF-style Q4 blocks -> the canonical packed int4 (q [rows][K/2], s fp16 bits)."""
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    rows = blocks.shape[0]
+    assert K % 32 == 0 and blocks.shape[1] == K // 32 * 18 and K % group == 0
+    q = np.empty((rows, K // 2), np.uint8)
+    s = np.empty((rows, K // group), np.uint16)
+    _get().orc_import_q4_blocks(_p(blocks), rows, K, group, _p(q), _p(s))
+    return q, s
+
 
 def router(x, W_r, bias, k: int, t0: int = 0, t1: int | None = None, threads: int = 1,
            want_scores: bool = False):

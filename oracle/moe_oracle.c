@@ -46,6 +46,11 @@
  *  R8 descriptors: perm lists slot ids t*k + j sorted by (expert, token);
  *     pos is its inverse; sched orders experts by count, largest first, ties
  *     to the lower id.
+ *  R15 GGUF-style Q4 block: 32 weights share one fp16 scale d (2 bytes,
+ *      little-endian) followed by 16 bytes of 4-bit codes n, weight i in bits
+ *      0-3 of byte i and weight i + 16 in bits 4-7; the weight is (n - 8) * d.
+ *      The import dequantises exactly (fp32 holds every (n - 8) * d) and then
+ *      packs with R1-R3 at the layer's group size.
  *  R14 residual add (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
  *      residual + routed + shared in one launch, routed and shared summed
  *      first): with a residual row r (bf16), out = bf16(float(r) + acc), where
@@ -174,6 +179,35 @@ void orc_dequant_w4(const uint8_t* q, const uint16_t* s, int64_t rows, int64_t K
         for (int64_t i = 0; i < K; ++i)
             w_hat[r * K + i] = (float)nibble_value(q + r * (K / 2), i) *
                                orc_f16_to_f32(s[r * ngroups + i / group]);
+}
+
+/* ------------------------------------------------------------------ */
+/* Load-time import of GGUF-style Q4 blocks (R15).                      */
+/* thewafflehaus/butter PR #69, commit "feat(laguna): Laguna-S-2.1       */
+/* decode on the CUDA engine": the expert weights are read from GGUF and */
+/* re-quantised to the engine's 4-bit format when the model is loaded.   */
+
+void orc_dequant_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, float* w) {
+    int64_t nb = K / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t* blk = blocks + (r * nb + b) * 18;
+            uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8)); /* little-endian fp16 */
+            float dscale = orc_f16_to_f32(dbits);
+            for (int i = 0; i < 32; ++i) {
+                int byte = blk[2 + (i & 15)];
+                int n = i < 16 ? (byte & 15) : (byte >> 4);
+                w[r * K + b * 32 + i] = (float)(n - 8) * dscale;
+            }
+        }
+}
+
+void orc_import_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, int32_t group,
+                          uint8_t* q, uint16_t* s) {
+    float* w = (float*)malloc(sizeof(float) * (size_t)(rows * K));
+    orc_dequant_q4_blocks(blocks, rows, K, w);
+    orc_pack_w4(w, rows, K, group, q, s);
+    free(w);
 }
 
 /* ------------------------------------------------------------------ */

@@ -36,6 +36,15 @@ void orc_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group, uint8_t
 void orc_dequant_w4(const uint8_t* q, const uint16_t* s, int64_t rows, int64_t K, int32_t group,
                     float* w_hat);
 
+/* GGUF-style Q4 blocks, 18 bytes per 32 weights of a row (K % 32 == 0):
+   an fp16 scale d (little-endian), then 16 bytes whose byte i holds the code
+   n of weight i in bits 0-3 and of weight i + 16 in bits 4-7; the weight is
+   (n - 8) * d.  orc_dequant_q4_blocks writes w [rows][K] (exact in fp32);
+   orc_import_q4_blocks re-quantises it with orc_pack_w4 at `group`. */
+void orc_dequant_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, float* w);
+void orc_import_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, int32_t group,
+                          uint8_t* q, uint16_t* s);
+
 /* Router for tokens [t0, t1): fp64 logits x . W_r[e], fp64 sigmoid scores s,
    top-k of s + bias (ties to lower id, descending), weights s_j / sum s_j.
    margin[t] = (k-th largest key) - ((k+1)-th largest key), +inf when k == E.

@@ -542,3 +542,44 @@ def test_residual_added_after_routed_plus_shared(oracle_lib):
     out = oracle_lib.layer(xb, Wr, b, W, k, residual=rb)["out"]
     assert np.array_equal(out, _bf16_bits(r + (routed + shared)))
     assert not np.array_equal(out[separating], _bf16_bits((r + routed) + shared)[separating])
+
+
+# ------------------------------------------------------------------ GGUF-style Q4 import
+
+
+def test_q4_blocks_hand_worked_fixture(oracle_lib):
+    g = read_golden("q4_block_example.txt")
+    K, group = int(g["K"][0][0]), int(g["group"][0][0])
+    block = np.array([int(v, 16) for v in g["block"][0]], np.uint8).reshape(1, 18)
+    w_ref = np.array([float(v) for row in g["w"] for v in row], np.float32).reshape(1, K)
+    assert np.array_equal(oracle_lib.dequant_q4_blocks(block, K), w_ref)
+    # the fixture's q and bytes agree with each other (element 2j in the low nibble)
+    qv = [int(v) for v in g["q"][0]]
+    assert [f"{(qv[2 * j] & 15) | ((qv[2 * j + 1] & 15) << 4):02X}" for j in range(K // 2)] \
+        == g["bytes"][0]
+    q, s = oracle_lib.import_q4_blocks(block, K, group)
+    assert q.tobytes().hex().upper() == "".join(g["bytes"][0])
+    assert [f"{v:04X}" for v in s[0]] == g["scales"][0]
+
+
+def test_q4_import_is_lossless_when_the_codes_fit(oracle_lib):
+    """Blocks whose codes avoid n = 0 and reach |n - 8| = 7: at group 32 the canonical
+    scale is |d| itself (7|d|/7 is exact in fp32) and q = +-(n - 8), so the import
+    loses nothing: q * s reproduces every block weight bit for bit."""
+    rng = np.random.default_rng(31)
+    rows, K = 6, 256
+    nb = K // 32
+    codes = rng.integers(1, 16, size=(rows, nb, 32))
+    codes[:, :, 0] = rng.choice([1, 15], size=(rows, nb))
+    mag = np.exp2(rng.integers(-10, 5, size=(rows, nb))) * (1 + rng.integers(0, 1024, (rows, nb)) / 1024)
+    d = (mag * rng.choice([-1.0, 1.0], size=(rows, nb))).astype(np.float16)
+    blocks = np.zeros((rows, nb, 18), np.uint8)
+    dbits = d.view(np.uint16)
+    blocks[:, :, 0] = dbits & 0xFF
+    blocks[:, :, 1] = dbits >> 8
+    blocks[:, :, 2:] = (codes[:, :, :16] | (codes[:, :, 16:] << 4)).astype(np.uint8)
+    blocks = blocks.reshape(rows, nb * 18)
+    w = oracle_lib.dequant_q4_blocks(blocks, K)
+    q, s = oracle_lib.import_q4_blocks(blocks, K, 32)
+    assert np.array_equal(oracle_lib.dequant_w4(q, s, 32), w)
+    assert np.array_equal(s, np.abs(d).view(np.uint16).reshape(rows, nb))
