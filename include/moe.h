@@ -127,6 +127,23 @@ moe_status_t moe_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group,
  * CUDA call.  Returns 0 (and writes 0) for arguments moe_pack_w4 rejects. */
 size_t moe_pack_w4_bytes(int64_t rows, int64_t K, int32_t group, size_t* scale_bytes);
 
+/* moe_import_q4_blocks -- load-time import of GGUF-style Q4 blocks into the
+ * packed int4 format above.  Source: the Q4 re-quantised weight load straight
+ * from GGUF of thewafflehaus/butter PR #69 (commit "feat(laguna): Laguna-S-2.1
+ * decode on the CUDA engine").  Block format (the GGUF Q4 block): 32 weights
+ * in 18 bytes, an fp16 scale d (little-endian) and then 16 bytes whose byte i
+ * holds the 4-bit code n of weight i in bits 0-3 and of weight i + 16 in bits
+ * 4-7; the weight is (n - 8) * d.  The import decodes every block exactly to
+ * fp32 in w_scratch, then quantises w_scratch as moe_pack_w4 does.
+ *   blocks    (device) uint8 [rows][K/32][18], row-major, any alignment
+ *   w_scratch (device) out: fp32 [rows][K], 16-byte aligned (left holding the
+ *             decoded weights)
+ *   q, s      (device) out: as moe_pack_w4 (q 4-byte, s 2-byte aligned)
+ * Requires K % 32 == 0 and K % group == 0, group as for moe_pack_w4.
+ */
+moe_status_t moe_import_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, int32_t group,
+                                  float* w_scratch, uint8_t* q, uint16_t* s, void* stream);
+
 /* Bytes of workspace the per-step calls below need for these dimensions
    (the same number serves every call; 0 on invalid dims). */
 size_t moe_workspace_bytes(const moe_dims_t* dims);

@@ -36,7 +36,7 @@ EXPORTS = (
     "moe_build_descriptors", "moe_gateup_swiglu_w4a16", "moe_down_w4a16", "moe_combine_shared",
     "moe_layer_workspace_bytes", "moe_layer_forward", "moe_layer_forward_host",
     "moe_check_device_status", "moe_router_topk_noalloc", "moe_pack_w4_bytes",
-    "moe_combine_shared_residual", "moe_layer_forward_residual",
+    "moe_combine_shared_residual", "moe_layer_forward_residual", "moe_import_q4_blocks",
 )
 
 
@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
         "moe_gateup_swiglu_w4a16": ([p, D, p, p, p, W4, W4, p, p, sz, p], i32),
         "moe_down_w4a16": ([p, D, p, p, W4, W4, p, p, sz, p], i32),
         "moe_pack_w4_bytes": ([i64, i64, i32, ctypes.POINTER(sz)], sz),
+        "moe_import_q4_blocks": ([p, i64, i64, i32, p, p, p, p], i32),
         "moe_combine_shared": ([p, p, p, D, p, p], i32),
         "moe_combine_shared_residual": ([p, p, p, D, p, p, p], i32),
         "moe_layer_forward_residual": ([p, p, p, D, W4, W4, W4, W4, p, p, p, sz, p], i32),
@@ -154,6 +155,28 @@ def moe_pack_w4(w: torch.Tensor, group: int, q: torch.Tensor | None = None,
                              _dev(q, torch.uint8, "q"), _dev(s, torch.int16, "s"),
                              _stream(stream)), "moe_pack_w4")
     return q, s
+
+
+def moe_import_q4_blocks(blocks: torch.Tensor, K: int, group: int, w_scratch=None,
+                         q: torch.Tensor | None = None, s: torch.Tensor | None = None,
+                         stream=None):
+    """GGUF-style Q4 blocks uint8 [rows][K/32*18] -> (q uint8 [rows][K/2], s fp16 bits as
+    int16 [rows][K/group], w_scratch fp32 [rows][K] holding the decoded weights)."""
+    rows = blocks.shape[0]
+    if blocks.dim() != 2 or blocks.shape[1] != (K // 32) * 18:
+        raise ValueError("blocks must be [rows][K/32*18] bytes")
+    dev = blocks.device
+    if w_scratch is None:
+        w_scratch = torch.empty((rows, K), dtype=torch.float32, device=dev)
+    if q is None:
+        q = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    if s is None:
+        s = torch.empty((rows, K // group), dtype=torch.int16, device=dev)
+    _check(lib().moe_import_q4_blocks(
+        _dev(blocks, torch.uint8, "blocks"), rows, K, group,
+        _dev(w_scratch, torch.float32, "w_scratch"), _dev(q, torch.uint8, "q"),
+        _dev(s, torch.int16, "s"), _stream(stream)), "moe_import_q4_blocks")
+    return q, s, w_scratch
 
 
 def moe_workspace_bytes(dims: Dims) -> int:

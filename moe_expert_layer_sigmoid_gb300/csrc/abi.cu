@@ -299,6 +299,20 @@ moe_status_t moe_pack_w4(const float* w, int64_t rows, int64_t K, int32_t group,
     return map_err(launch_pack_w4(w, rows, K, group, q, s, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_import_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, int32_t group,
+                                  float* w_scratch, uint8_t* q, uint16_t* s, void* stream) {
+    if (rows < 0 || K <= 0 || group <= 0) return MOE_ERR_INVALID_ARG;
+    if (!(group == 8 || group == 16 || group_ok(group))) return MOE_ERR_UNSUPPORTED;
+    if (K % 32 || K % group) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !act_ok(w_scratch) || !q || !s) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(q) % 4 || reinterpret_cast<uintptr_t>(s) % 2)
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (launch_decode_q4_blocks(blocks, rows, K, w_scratch, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return map_err(launch_pack_w4(w_scratch, rows, K, group, q, s, st));
+}
+
 size_t moe_workspace_bytes(const moe_dims_t* dims) {
     if (check_dims(dims) != MOE_OK) return 0;
     return ws_layout(*dims).step_bytes;

@@ -87,6 +87,9 @@ bool act_ok(const void* p);  // non-null and 16-byte aligned
 // cudaGetLastError of the launch.
 cudaError_t launch_pack_w4(const float* w, int64_t rows, int64_t K, int group, uint8_t* q,
                            uint16_t* s, cudaStream_t st);
+// GGUF-style Q4 blocks [rows][K/32][18 B] -> fp32 w [rows][K] (K % 32 == 0).
+cudaError_t launch_decode_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, float* w,
+                                    cudaStream_t st);
 
 // Router: logits as split-K partials (ksplit slices for T <= kRouterSmallT,
 // ksplit_large above it), then the top-k.

@@ -53,7 +53,40 @@ __global__ void __launch_bounds__(256) pack_w4_kernel(const float* __restrict__ 
     s[gid] = sh;
 }
 
+// GGUF-style Q4 blocks -> fp32 rows (load-time import; the weights are read
+// from GGUF and re-quantised at load in the same commit).  A block is 18
+// bytes: an fp16 scale d (little-endian) and 16 bytes whose byte i holds the
+// code n of weight i in bits 0-3 and of weight i + 16 in bits 4-7; the
+// weight is (n - 8) * d, exact in fp32.  One thread per block; blocks are
+// row-major, so block b covers w[32 b .. 32 b + 31].  Bytes are read one at a
+// time: a block is only 2-byte aligned.
+__global__ void __launch_bounds__(256) q4_blocks_decode_kernel(const uint8_t* __restrict__ blocks,
+                                                               int64_t nblocks,
+                                                               float* __restrict__ w) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const uint8_t* blk = blocks + b * 18;
+    const float d = __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
+    float* out = w + b * 32;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int byte = blk[2 + i];
+        out[i] = (float)((byte & 15) - 8) * d;
+        out[i + 16] = (float)((byte >> 4) - 8) * d;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_decode_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, float* w,
+                                    cudaStream_t st) {
+    const int64_t nblocks = rows * (K / 32);
+    if (nblocks == 0) return cudaSuccess;
+    const int threads = 256;
+    const unsigned grid = (unsigned)((nblocks + threads - 1) / threads);
+    q4_blocks_decode_kernel<<<grid, threads, 0, st>>>(blocks, nblocks, w);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack_w4(const float* w, int64_t rows, int64_t K, int group, uint8_t* q,
                            uint16_t* s, cudaStream_t st) {

@@ -178,3 +178,16 @@ def test_misaligned_activation_pointers_rejected(L):
                                None) == INV
     assert L.moe_layer_forward(ok, ok, ok, ctypes.byref(d), w4, w4, w4, w4, bad, ws, layer,
                                None) == INV
+
+
+def test_import_q4_blocks_validation(L):
+    ok = 1 << 21
+    INV, UNS = moe.MOE_ERR_INVALID_ARG, moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_import_q4_blocks(None, 0, 64, 32, None, None, None, None) == moe.MOE_OK
+    assert L.moe_import_q4_blocks(ok, 2, 48, 16, ok, ok, ok, None) == INV      # K % 32
+    assert L.moe_import_q4_blocks(ok, 2, 96, 64, ok, ok, ok, None) == INV      # K % group
+    assert L.moe_import_q4_blocks(ok, 2, 96, 48, ok, ok, ok, None) == UNS      # group
+    assert L.moe_import_q4_blocks(ok, -1, 64, 32, ok, ok, ok, None) == INV
+    assert L.moe_import_q4_blocks(None, 2, 64, 32, ok, ok, ok, None) == INV
+    assert L.moe_import_q4_blocks(ok, 2, 64, 32, ok + 4, ok, ok, None) == INV  # w_scratch align
+    assert L.moe_import_q4_blocks(ok, 2, 64, 32, ok, ok + 2, ok, None) == INV  # q align
