@@ -133,8 +133,13 @@ size_t moe_pack_w4_bytes(int64_t rows, int64_t K, int32_t group, size_t* scale_b
  * decode on the CUDA engine").  Block format (the GGUF Q4 block): 32 weights
  * in 18 bytes, an fp16 scale d (little-endian) and then 16 bytes whose byte i
  * holds the 4-bit code n of weight i in bits 0-3 and of weight i + 16 in bits
- * 4-7; the weight is (n - 8) * d.  The import decodes every block exactly to
- * fp32 in w_scratch, then quantises w_scratch as moe_pack_w4 does.
+ * 4-7; the weight is (n - 8) * d.  With group <= 32 every quantisation group
+ * lies inside one block and the import is exact: s = d (its fp16 bits, sign
+ * included) and q = n - 8.  With group 64 or 128 a group spans blocks with
+ * different scales, so the import decodes every block exactly to fp32 in
+ * w_scratch and then quantises w_scratch as moe_pack_w4 does (s = absmax / 7
+ * per group; lossy wherever a group's blocks do not share one scale grid).
+ * Either way w_scratch is left holding the decoded weights.
  *   blocks    (device) uint8 [rows][K/32][18], row-major, any alignment
  *   w_scratch (device) out: fp32 [rows][K], 16-byte aligned (left holding the
  *             decoded weights)

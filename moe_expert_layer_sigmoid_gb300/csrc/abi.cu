@@ -309,6 +309,8 @@ moe_status_t moe_import_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K
     if (reinterpret_cast<uintptr_t>(q) % 4 || reinterpret_cast<uintptr_t>(s) % 2)
         return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (group <= 32)  // each group inside one block: s = d, q = n - 8, exact
+        return map_err(launch_import_q4_direct(blocks, rows, K, group, w_scratch, q, s, st));
     if (launch_decode_q4_blocks(blocks, rows, K, w_scratch, st) != cudaSuccess) return MOE_ERR_CUDA;
     return map_err(launch_pack_w4(w_scratch, rows, K, group, q, s, st));
 }

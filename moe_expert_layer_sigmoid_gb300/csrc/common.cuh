@@ -90,6 +90,10 @@ cudaError_t launch_pack_w4(const float* w, int64_t rows, int64_t K, int group, u
 // GGUF-style Q4 blocks [rows][K/32][18 B] -> fp32 w [rows][K] (K % 32 == 0).
 cudaError_t launch_decode_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, float* w,
                                     cudaStream_t st);
+// GGUF-style Q4 blocks straight to the packed format for group <= 32 (s = d,
+// q = n - 8, exact), also writing the decoded fp32 weights to w.
+cudaError_t launch_import_q4_direct(const uint8_t* blocks, int64_t rows, int64_t K, int group,
+                                    float* w, uint8_t* q, uint16_t* s, cudaStream_t st);
 
 // Router: logits as split-K partials (ksplit slices for T <= kRouterSmallT,
 // ksplit_large above it), then the top-k.

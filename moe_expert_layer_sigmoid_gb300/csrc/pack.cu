@@ -76,7 +76,53 @@ __global__ void __launch_bounds__(256) q4_blocks_decode_kernel(const uint8_t* __
     }
 }
 
+// Groups of at most 32 lie inside one block, so the block is already in the
+// canonical form: s = d (its fp16 bits), q = n - 8, whose two's-complement
+// nibble is n ^ 8.  One thread per block: 16 packed bytes (element 2j low),
+// 32 / G scales, and the decoded fp32 weights for w_scratch.
+template <int G>
+__global__ void __launch_bounds__(256) q4_blocks_direct_kernel(const uint8_t* __restrict__ blocks,
+                                                               int64_t nblocks, float* __restrict__ w,
+                                                               uint8_t* __restrict__ q,
+                                                               uint16_t* __restrict__ s) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const uint8_t* blk = blocks + b * 18;
+    const uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    const float d = __half2float(__ushort_as_half(dbits));
+    uint8_t n[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int byte = blk[2 + i];
+        n[i] = (uint8_t)(byte & 15);
+        n[i + 16] = (uint8_t)(byte >> 4);
+    }
+    uint8_t* qo = q + b * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) qo[j] = (uint8_t)((n[2 * j] ^ 8) | ((n[2 * j + 1] ^ 8) << 4));
+#pragma unroll
+    for (int i = 0; i < 32 / G; ++i) s[b * (32 / G) + i] = dbits;
+    float* out = w + b * 32;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) out[i] = (float)((int)n[i] - 8) * d;
+}
+
 }  // namespace
+
+cudaError_t launch_import_q4_direct(const uint8_t* blocks, int64_t rows, int64_t K, int group,
+                                    float* w, uint8_t* q, uint16_t* s, cudaStream_t st) {
+    const int64_t nblocks = rows * (K / 32);
+    if (nblocks == 0) return cudaSuccess;
+    const int threads = 256;
+    const unsigned grid = (unsigned)((nblocks + threads - 1) / threads);
+    switch (group) {
+        case 8: q4_blocks_direct_kernel<8><<<grid, threads, 0, st>>>(blocks, nblocks, w, q, s); break;
+        case 16: q4_blocks_direct_kernel<16><<<grid, threads, 0, st>>>(blocks, nblocks, w, q, s); break;
+        case 32: q4_blocks_direct_kernel<32><<<grid, threads, 0, st>>>(blocks, nblocks, w, q, s); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, float* w,
                                     cudaStream_t st) {

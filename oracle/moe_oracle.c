@@ -49,8 +49,11 @@
  *  R15 GGUF-style Q4 block: 32 weights share one fp16 scale d (2 bytes,
  *      little-endian) followed by 16 bytes of 4-bit codes n, weight i in bits
  *      0-3 of byte i and weight i + 16 in bits 4-7; the weight is (n - 8) * d.
- *      The import dequantises exactly (fp32 holds every (n - 8) * d) and then
- *      packs with R1-R3 at the layer's group size.
+ *      The import keeps the weights exact where the canonical format can:
+ *      with a group of at most 32 every group lies inside one block, so
+ *      s = d (its fp16 bits) and q = n - 8, which is already in [-8, 7].  A
+ *      group of 64 or 128 spans blocks with different scales: those rows are
+ *      decoded exactly (fp32 holds every (n - 8) * d) and packed with R1-R3.
  *  R14 residual add (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
  *      residual + routed + shared in one launch, routed and shared summed
  *      first): with a residual row r (bf16), out = bf16(float(r) + acc), where
@@ -204,6 +207,23 @@ void orc_dequant_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, float
 
 void orc_import_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, int32_t group,
                           uint8_t* q, uint16_t* s) {
+    if (group <= 32) {  /* every group inside one block: s = d, q = n - 8 */
+        int64_t nb = K / 32, ng = K / group;
+        for (int64_t r = 0; r < rows; ++r)
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* blk = blocks + (r * nb + b) * 18;
+                uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+                for (int i = 0; i < 32; i += group) s[r * ng + (b * 32 + i) / group] = dbits;
+                for (int j = 0; j < 16; ++j) {
+                    int e0 = 2 * j, e1 = 2 * j + 1; /* elements of packed byte j */
+                    int n0 = e0 < 16 ? (blk[2 + e0] & 15) : (blk[2 + e0 - 16] >> 4);
+                    int n1 = e1 < 16 ? (blk[2 + e1] & 15) : (blk[2 + e1 - 16] >> 4);
+                    int q0 = n0 - 8, q1 = n1 - 8; /* two's-complement nibbles */
+                    q[r * (K / 2) + b * 16 + j] = (uint8_t)((q0 & 15) | ((q1 & 15) << 4));
+                }
+            }
+        return;
+    }
     float* w = (float*)malloc(sizeof(float) * (size_t)(rows * K));
     orc_dequant_q4_blocks(blocks, rows, K, w);
     orc_pack_w4(w, rows, K, group, q, s);

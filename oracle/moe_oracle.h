@@ -40,7 +40,8 @@ void orc_dequant_w4(const uint8_t* q, const uint16_t* s, int64_t rows, int64_t K
    an fp16 scale d (little-endian), then 16 bytes whose byte i holds the code
    n of weight i in bits 0-3 and of weight i + 16 in bits 4-7; the weight is
    (n - 8) * d.  orc_dequant_q4_blocks writes w [rows][K] (exact in fp32);
-   orc_import_q4_blocks re-quantises it with orc_pack_w4 at `group`. */
+   orc_import_q4_blocks packs it at `group`: for group <= 32 exactly (s = d,
+   q = n - 8), for group 64 / 128 by re-quantising w with orc_pack_w4. */
 void orc_dequant_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, float* w);
 void orc_import_q4_blocks(const uint8_t* blocks, int64_t rows, int64_t K, int32_t group,
                           uint8_t* q, uint16_t* s);

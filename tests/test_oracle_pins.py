@@ -549,6 +549,7 @@ def test_residual_added_after_routed_plus_shared(oracle_lib):
 
 def test_q4_blocks_hand_worked_fixture(oracle_lib):
     g = read_golden("q4_block_example.txt")
+    # case A: group 32, the block kept exactly (s = d, q = n - 8)
     K, group = int(g["K"][0][0]), int(g["group"][0][0])
     block = np.array([int(v, 16) for v in g["block"][0]], np.uint8).reshape(1, 18)
     w_ref = np.array([float(v) for row in g["w"] for v in row], np.float32).reshape(1, K)
@@ -560,17 +561,22 @@ def test_q4_blocks_hand_worked_fixture(oracle_lib):
     q, s = oracle_lib.import_q4_blocks(block, K, group)
     assert q.tobytes().hex().upper() == "".join(g["bytes"][0])
     assert [f"{v:04X}" for v in s[0]] == g["scales"][0]
+    assert np.array_equal(oracle_lib.dequant_w4(q, s, group), w_ref)
+    # case B: group 64 over two blocks, re-quantised at absmax / 7
+    K, group = int(g["K64"][0][0]), int(g["group64"][0][0])
+    block = np.array([int(v, 16) for v in g["block64"][0]], np.uint8).reshape(1, 36)
+    qv = [int(v) for row in g["q64"] for v in row]
+    assert [f"{(qv[2 * j] & 15) | ((qv[2 * j + 1] & 15) << 4):02X}" for j in range(K // 2)] \
+        == g["bytes64"][0]
+    q, s = oracle_lib.import_q4_blocks(block, K, group)
+    assert q.tobytes().hex().upper() == "".join(g["bytes64"][0])
+    assert [f"{v:04X}" for v in s[0]] == g["scales64"][0]
 
 
-def test_q4_import_is_lossless_when_the_codes_fit(oracle_lib):
-    """Blocks whose codes avoid n = 0 and reach |n - 8| = 7: at group 32 the canonical
-    scale is |d| itself (7|d|/7 is exact in fp32) and q = +-(n - 8), so the import
-    loses nothing: q * s reproduces every block weight bit for bit."""
-    rng = np.random.default_rng(31)
-    rows, K = 6, 256
+def _q4_blocks(rng, rows, K, codes=None):
     nb = K // 32
-    codes = rng.integers(1, 16, size=(rows, nb, 32))
-    codes[:, :, 0] = rng.choice([1, 15], size=(rows, nb))
+    if codes is None:
+        codes = rng.integers(0, 16, size=(rows, nb, 32))
     mag = np.exp2(rng.integers(-10, 5, size=(rows, nb))) * (1 + rng.integers(0, 1024, (rows, nb)) / 1024)
     d = (mag * rng.choice([-1.0, 1.0], size=(rows, nb))).astype(np.float16)
     blocks = np.zeros((rows, nb, 18), np.uint8)
@@ -578,8 +584,36 @@ def test_q4_import_is_lossless_when_the_codes_fit(oracle_lib):
     blocks[:, :, 0] = dbits & 0xFF
     blocks[:, :, 1] = dbits >> 8
     blocks[:, :, 2:] = (codes[:, :, :16] | (codes[:, :, 16:] << 4)).astype(np.uint8)
-    blocks = blocks.reshape(rows, nb * 18)
+    return blocks.reshape(rows, nb * 18), d, codes
+
+
+@pytest.mark.parametrize("group", [8, 16, 32])
+def test_q4_import_is_exact_at_groups_within_a_block(oracle_lib, group):
+    """At a group of at most 32 the import is lossless for every code, n = 0 (q = -8)
+    included, and for scales of either sign: q * s reproduces every block weight bit
+    for bit, the scales are d's bits and the nibbles are n ^ 8."""
+    rng = np.random.default_rng(31 + group)
+    rows, K = 6, 256
+    codes = rng.integers(0, 16, size=(rows, K // 32, 32))
+    codes[:, :, 0] = 0  # every block holds the weight -8 * d
+    blocks, d, codes = _q4_blocks(rng, rows, K, codes)
     w = oracle_lib.dequant_q4_blocks(blocks, K)
-    q, s = oracle_lib.import_q4_blocks(blocks, K, 32)
-    assert np.array_equal(oracle_lib.dequant_w4(q, s, 32), w)
-    assert np.array_equal(s, np.abs(d).view(np.uint16).reshape(rows, nb))
+    q, s = oracle_lib.import_q4_blocks(blocks, K, group)
+    assert np.array_equal(oracle_lib.dequant_w4(q, s, group), w)
+    assert np.array_equal(s, np.repeat(d.view(np.uint16), 32 // group, axis=1))
+    flat = codes.reshape(rows, K)  # element e of a block: code index e
+    assert np.array_equal(q & 15, (flat[:, 0::2] ^ 8).astype(np.uint8))
+    assert np.array_equal(q >> 4, (flat[:, 1::2] ^ 8).astype(np.uint8))
+
+
+def test_q4_import_requantises_groups_spanning_blocks(oracle_lib):
+    """At group 64 / 128 a group spans blocks with their own scales: the rows are
+    decoded exactly and packed as moe_pack_w4 packs fp32 weights."""
+    rng = np.random.default_rng(77)
+    rows, K = 4, 512
+    blocks, _, _ = _q4_blocks(rng, rows, K)
+    w = oracle_lib.dequant_q4_blocks(blocks, K)
+    for group in (64, 128):
+        q, s = oracle_lib.import_q4_blocks(blocks, K, group)
+        qp, sp = oracle_lib.pack_w4(w, group)
+        assert np.array_equal(q, qp) and np.array_equal(s, sp)

@@ -1,6 +1,7 @@
 """GPU: the load-time import of GGUF-style Q4 blocks through the C ABI
 (moe_import_q4_blocks) against the oracle, bit for bit: the decoded fp32
-weights, the packed int4 bytes and the fp16 scales.  The block layout and the
+weights, the packed int4 bytes and the fp16 scales, at groups inside one block
+(8, 16, 32: the block kept exactly) and across blocks (64, 128: re-quantised).  The block layout and the
 import follow the oracle's reading R15 (the Q4 weight load from GGUF of
 thewafflehaus/butter PR #69, commit "feat(laguna): Laguna-S-2.1 decode on the
 CUDA engine")."""
@@ -28,8 +29,8 @@ def random_blocks(rng, rows, K):
     return blocks.reshape(rows, nb * 18)
 
 
-@pytest.mark.parametrize("rows,K,g", [(1, 32, 32), (3, 96, 32), (5, 256, 128), (7, 384, 64),
-                                      (33, 4096, 128)])
+@pytest.mark.parametrize("rows,K,g", [(1, 32, 32), (3, 96, 32), (2, 64, 8), (4, 160, 16),
+                                      (5, 256, 128), (7, 384, 64), (33, 4096, 128)])
 def test_import_matches_oracle(rows, K, g):
     rng = np.random.default_rng(rows * 1000 + K + g)
     blocks = random_blocks(rng, rows, K)
@@ -41,12 +42,15 @@ def test_import_matches_oracle(rows, K, g):
     assert np.array_equal(s.cpu().numpy().view(np.uint16), so)
 
 
-def test_import_hand_worked_fixture_on_gpu():
+@pytest.mark.parametrize("sfx,nbytes", [("", 18), ("64", 36)])
+def test_import_hand_worked_fixture_on_gpu(sfx, nbytes):
+    """Case A (group 32: the block kept exactly) and case B (group 64 across two
+    blocks: re-quantised)."""
     from conftest import read_golden
     gold = read_golden("q4_block_example.txt")
-    K, g = int(gold["K"][0][0]), int(gold["group"][0][0])
-    block = np.array([int(v, 16) for v in gold["block"][0]], np.uint8).reshape(1, 18)
+    K, g = int(gold["K" + sfx][0][0]), int(gold["group" + sfx][0][0])
+    block = np.array([int(v, 16) for v in gold["block" + sfx][0]], np.uint8).reshape(1, nbytes)
     q, s, _ = moe.moe_import_q4_blocks(torch.from_numpy(block).cuda(), K, g)
     torch.cuda.synchronize()
-    assert q.cpu().numpy().tobytes().hex().upper() == "".join(gold["bytes"][0])
-    assert [f"{v:04X}" for v in s.cpu().numpy().view(np.uint16)[0]] == gold["scales"][0]
+    assert q.cpu().numpy().tobytes().hex().upper() == "".join(gold["bytes" + sfx][0])
+    assert [f"{v:04X}" for v in s.cpu().numpy().view(np.uint16)[0]] == gold["scales" + sfx][0]
