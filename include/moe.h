@@ -190,8 +190,16 @@ moe_status_t moe_router_topk(const uint16_t* x, const float* W_r, const float* b
  *    4 MiB returns MOE_ERR_UNSUPPORTED before launching.  For E = 256 that is
  *    T <= 64 in the decode form (at d <= 16384) and T <= 4096 above it.
  *  - Set-up: the first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it.  Make
- *    that first call before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and caches it.  With
+ *    lazy module loading (CUDA_MODULE_LOADING=LAZY, the default of current CUDA
+ *    runtimes) that lookup is also what loads the array's module, so the 4 MiB
+ *    are allocated on the device by that first call, not when the library is
+ *    loaded.  A caller that reserves all of HBM must therefore make one call on
+ *    each device first (a T = 1 call is enough), or run with
+ *    CUDA_MODULE_LOADING=EAGER so that the array is allocated when the library
+ *    loads.  Make the first call before any stream capture too.
+ *  - Devices: the cached address belongs to the current device (cudaGetDevice)
+ *    at the time of the call, so `stream` must be a stream of that device.
  *  - Sharing: every call uses the same array.  The call writes every partial
  *    it reads, so nothing needs clearing between calls.  Calls that overlap on
  *    the GPU (concurrent streams, or several host threads on one device)

@@ -12,7 +12,11 @@
 // Host code must not pass the array's name to a kernel: on the host that name
 // is a stand-in symbol, not a device address.  On each device the first call
 // looks up the array's device address with cudaGetSymbolAddress, with that
-// device current, and caches it.
+// device current, and caches it.  Under lazy module loading (the runtime's
+// default) that lookup is what loads this file's module, so the array is
+// allocated by the first call on each device: callers that reserve all of HBM
+// make one call per device first, or set CUDA_MODULE_LOADING=EAGER.  The
+// address is the current device's, so the caller's stream must belong to it.
 #include <mutex>
 
 #include "common.cuh"

@@ -54,9 +54,14 @@ def test_noalloc_router_matches_workspace_router_on_two_calls(cfg):
         x = torch.from_numpy(workloads.gen_x(cfg, batch=call).view(np.int16)).cuda()
         i_ref, w_ref, m_ref = _route(cfg, x, wr, b, noalloc=False)
         i_got, w_got, m_got = _route(cfg, x, wr, b, noalloc=True)
-        assert np.array_equal(i_got, i_ref), f"call {call}: expert ids differ"
-        assert np.max(np.abs(w_got - w_ref)) <= 2e-6, f"call {call}: weights differ"
-        assert np.max(np.abs(m_got - m_ref)) <= 1e-5, f"call {call}: margins differ"
+        # the two forms may sum the logit partials in a different order (the
+        # workspace form splits K above 64 tokens), so a token whose top-k margin
+        # is below 1e-5 may select differently: the matching rule leaves it out
+        keep = (m_ref >= 1e-5) & (m_got >= 1e-5)
+        assert keep.sum() >= cfg.T - 2, f"call {call}: too many near-ties"
+        assert np.array_equal(i_got[keep], i_ref[keep]), f"call {call}: expert ids differ"
+        assert np.max(np.abs(w_got[keep] - w_ref[keep])) <= 2e-6, f"call {call}: weights differ"
+        assert np.max(np.abs(m_got[keep] - m_ref[keep])) <= 1e-5, f"call {call}: margins differ"
 
 
 def test_noalloc_router_rejects_sizes_beyond_its_scratch():
