@@ -95,6 +95,9 @@ typedef struct {
 #define MOE_FLAG_FORCE_GEMV 0x1u    /* run the experts on the CUDA-core GEMV path     */
 #define MOE_FLAG_FORCE_GROUPED 0x2u /* run the experts on the tcgen05 grouped path    */
 #define MOE_FLAG_NO_SCHED 0x4u      /* grouped path: expert-id order, no N-banding     */
+#define MOE_FLAG_DECODE_MMA 0x8u    /* T = 1 on the GEMV path: the warp-level tensor-core
+                                       projections (one cooperative launch for the whole
+                                       layer) instead of the CUDA-core GEMVs              */
 
 /* Packed int4 weights: q [rows][K/2] bytes, s [rows][K/group] fp16 (device);
    q 16-byte aligned, s 2-byte aligned (MOE_ERR_INVALID_ARG otherwise). */

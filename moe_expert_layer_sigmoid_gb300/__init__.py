@@ -29,6 +29,7 @@ MOE_ERR_DEVICE_CHECK = 5
 MOE_FLAG_FORCE_GEMV = 0x1
 MOE_FLAG_FORCE_GROUPED = 0x2
 MOE_FLAG_NO_SCHED = 0x4
+MOE_FLAG_DECODE_MMA = 0x8
 
 # every extern "C" symbol include/moe.h declares
 EXPORTS = (

@@ -173,6 +173,9 @@ moe_status_t gateup_impl(const uint16_t* x, const moe_dims_t& d, const int32_t* 
     WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
     switch (expert_path(d)) {
         case Path::kGemv:
+            if ((d.flags & MOE_FLAG_DECODE_MMA) && tc_decode_supported(d) && tc_weights_ok(Wgu, Wgu_s))
+                return map_err(launch_gateup_tc(x, d, offsets, sched, Wgu, Wgu_s, H, nullptr, hdr,
+                                                false, st));
             return map_err(launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, nullptr,
                                               hdr, false, st));
         case Path::kGrouped:
@@ -190,6 +193,9 @@ moe_status_t down_impl(const uint16_t* H, const moe_dims_t& d, const int32_t* of
     WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
     switch (expert_path(d)) {
         case Path::kGemv:
+            if ((d.flags & MOE_FLAG_DECODE_MMA) && tc_decode_supported(d) && tc_weights_ok(Wd, Wd_s))
+                return map_err(launch_down_tc(H, d, offsets, sched, Wd, Wd_s, Y, nullptr, nullptr,
+                                              nullptr, nullptr, nullptr, false, st));
             return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, nullptr, nullptr,
                                             nullptr, nullptr, nullptr, hdr, false, st));
         case Path::kGrouped:
@@ -227,6 +233,14 @@ moe_status_t layer_forward(const uint16_t* x, const float* W_r, const float* bia
     const Path path = expert_path(d);
     if (path == Path::kUnsupported) return MOE_ERR_UNSUPPORTED;
     cudaError_t e;
+    const bool tc_w = (d.flags & MOE_FLAG_DECODE_MMA) && tc_weights_ok(Wgu, Wgu_s) &&
+                      tc_weights_ok(Wd, Wd_s);
+    if (path == Path::kGemv && d.T == 1 && tc_w && step_supported(d)) {
+        // the single-token step in one cooperative launch
+        return map_err(launch_decode_step(x, W_r, bias, d, topk_idx, topk_w, counts, offsets, perm,
+                                          pos, sched, ws_at<float>(ws, L.logits), L.router_ksplit,
+                                          Wgu, Wd, Wgu_s, Wd_s, H, residual, out, hdr, s));
+    }
     if (path == Path::kGemv) {
         // decode chain: fused router + descriptors, then the two GEMVs with the
         // combine fused into the down kernel; each waits on its predecessor
@@ -244,6 +258,12 @@ moe_status_t layer_forward(const uint16_t* x, const float* W_r, const float* bia
                                    ws_at<int4>(ws, L.tiles), L.max_tiles,
                                    ws_at<int32_t>(ws, L.hist), s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
+        }
+        if (tc_w && tc_decode_supported(d)) {
+            e = launch_gateup_tc(x, d, offsets, sched, Wgu, Wgu_s, H, &hdr->n_active, hdr, true, s);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            return map_err(launch_down_tc(H, d, offsets, sched, Wd, Wd_s, Y, &hdr->n_active,
+                                          topk_w, pos, residual, out, true, s));
         }
         e = launch_gateup_gemv(x, d, offsets, perm, sched, Wgu, Wgu_s, H, &hdr->n_active, hdr,
                                true, s);

@@ -27,7 +27,8 @@ struct WsHeader {
     int32_t error_flags;   // OR of kErr* bits; cleared by moe_check_device_status
     int32_t n_active;      // routed experts with count > 0 (written by the descriptors)
     int32_t n_tiles[2];    // grouped-GEMM tile counts: [0] gate+up, [1] down
-    int32_t done[4];       // arrival counters; [0]: CTAs of router_decode_kernel (the last resets it)
+    int32_t done[4];       // arrival counters; [0]: CTAs of router_decode_kernel (the last resets it);
+                           // [2..3]: the single-launch step's 64-bit grid-barrier arrival count
     int32_t pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
@@ -67,6 +68,28 @@ constexpr int kRouterSmallT = 64;
 constexpr int kGemvMaxT = 4;
 constexpr int kGemvMaxD = 4096;
 constexpr int kGemvMaxF = 2048;
+
+// Single-token expert projections on the warp-level tensor cores
+// (decode_tc.cu); taken for T == 1 on the GEMV path when the shapes fit.
+bool tc_decode_supported(const moe_dims_t& d);
+bool tc_weights_ok(moe_w4_t a, moe_w4_t b);  // 16-byte aligned bytes and scales
+cudaError_t launch_gateup_tc(const uint16_t* x, const moe_dims_t& d, const int32_t* offsets,
+                             const int32_t* sched, moe_w4_t Wgu, moe_w4_t Wgu_s, uint16_t* H,
+                             const int32_t* n_active, WsHeader* hdr, bool pdl, cudaStream_t st);
+cudaError_t launch_down_tc(const uint16_t* H, const moe_dims_t& d, const int32_t* offsets,
+                           const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y,
+                           const int32_t* n_active, const float* topk_w, const int32_t* pos,
+                           const uint16_t* residual, uint16_t* out, bool pdl, cudaStream_t st);
+
+// The whole single-token step in one cooperative launch (decode_tc.cu):
+// router, descriptors, both projections and the combine.
+bool step_supported(const moe_dims_t& d);
+cudaError_t launch_decode_step(const uint16_t* x, const float* W_r, const float* bias,
+                               const moe_dims_t& d, int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
+                               int32_t* sched, float* logits, int ksplit, moe_w4_t Wgu, moe_w4_t Wd,
+                               moe_w4_t Wgu_s, moe_w4_t Wd_s, uint16_t* H, const uint16_t* residual,
+                               uint16_t* out, WsHeader* hdr, cudaStream_t st);
 
 // Fused decode router (decode.cu) limits.
 constexpr int kMaxDecodeT = 64;

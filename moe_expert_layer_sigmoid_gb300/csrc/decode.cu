@@ -131,29 +131,6 @@ __device__ __forceinline__ void topk_rank_block(const DecodeRouterArgs& a, int k
     __syncthreads();
 }
 
-// Bitonic sort of one (key, e, v) per lane across a warp.  DESC: best first
-// by (key, then lower e); otherwise by ascending e alone.
-template <bool DESC>
-__device__ __forceinline__ void warp_bitonic(float& key, int& e, float& v, int lane) {
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const float pk = __shfl_xor_sync(0xffffffffu, key, stride);
-            const int pe = __shfl_xor_sync(0xffffffffu, e, stride);
-            const float pv = __shfl_xor_sync(0xffffffffu, v, stride);
-            const bool partner_first = DESC ? router_better(pk, pe, key, e) : pe < e;
-            const bool lower = (lane & stride) == 0;
-            const bool dir = (lane & size) == 0;  // this run is sorted first-to-last
-            if (lower == dir ? partner_first : !partner_first) {
-                key = pk;
-                e = pe;
-                v = pv;
-            }
-        }
-    }
-}
-
 // Single token, E <= 256: one expert per thread.  Each warp sorts its 32 keys
 // and keeps its best k + 1 as candidates; a candidate's rank among all
 // candidates is its rank among all experts (an expert outside its warp's best

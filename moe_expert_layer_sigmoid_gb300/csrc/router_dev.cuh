@@ -101,6 +101,29 @@ __device__ __forceinline__ RouterCand router_warp_argmax(RouterCand c) {
     return c;
 }
 
+// Bitonic sort of one (key, e, v) per lane across a warp.  DESC: best first
+// by (key, then lower e); otherwise by ascending e alone.
+template <bool DESC>
+__device__ __forceinline__ void warp_bitonic(float& key, int& e, float& v, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float pk = __shfl_xor_sync(0xffffffffu, key, stride);
+            const int pe = __shfl_xor_sync(0xffffffffu, e, stride);
+            const float pv = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool partner_first = DESC ? router_better(pk, pe, key, e) : pe < e;
+            const bool lower = (lane & stride) == 0;
+            const bool dir = (lane & size) == 0;  // this run is sorted first-to-last
+            if (lower == dir ? partner_first : !partner_first) {
+                key = pk;
+                e = pe;
+                v = pv;
+            }
+        }
+    }
+}
+
 // Top-k of token t, one warp; lane l holds experts l, l + 32, ...  The logit
 // of expert e is the sum of its ksplit partials in kc order.  Selection is k
 // rounds of a warp arg-max of s + bias (ties to the lower id).  Lane j < k
