@@ -32,6 +32,13 @@
  *    of trapping; moe_check_device_status reads it.
  *  - T = 0 is valid: the call validates the other arguments, returns MOE_OK
  *    and enqueues nothing.
+ *  - Determinism: every call is deterministic, always: the same inputs on the
+ *    same flags and shapes give the same bits, run after run.  No kernel uses
+ *    floating-point atomics or an order that depends on timing; every sum is
+ *    taken in a fixed order.  So there is no switch for it (the pages' MoE
+ *    keeps a deterministic scatter-add for the same reason).  Different paths
+ *    (flags, or T on either side of the path crossover) sum in different
+ *    orders and may differ in the last bits.
  *
  * Numerics (the reading of the layer statement this library implements)
  *  - int4 weights: per row, per group of `group` consecutive K elements,
@@ -263,8 +270,14 @@ moe_status_t moe_gateup_swiglu_w4a16(const uint16_t* x, const moe_dims_t* dims,
                                      uint16_t* H, void* ws, size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------------------------
- * moe_down_w4a16 -- down projection of every row of H.
- * Source: the per-expert down projection of the same pages' MoE layer.
+ * moe_down_w4a16 -- down projection of every row of H (routed rows with their
+ * expert's down weights, the shared rows with the shared expert's).  Sources:
+ * the gathered Q4 down GEMV of the decode step, thewafflehaus/butter PR #69,
+ * commit "feat(laguna): Laguna-S-2.1 decode on the CUDA engine"; the
+ * per-expert down projection of the W4A16 grouped MoE, thewafflehaus/FFAI
+ * PR #72, Nemotron W4A16 Marlin MoE commit.  H rows are already grouped by
+ * expert (descriptor order), so no gather is needed and perm is not an
+ * argument.
  *   H        (device) bf16 [T*k + T][max(F, F_s)]
  *   offsets, sched (device) from moe_build_descriptors
  *   Wd       routed down, q [E][d][F/2], s [E][d][F/group]
@@ -275,6 +288,29 @@ moe_status_t moe_gateup_swiglu_w4a16(const uint16_t* x, const moe_dims_t* dims,
 moe_status_t moe_down_w4a16(const uint16_t* H, const moe_dims_t* dims, const int32_t* offsets,
                             const int32_t* sched, moe_w4_t Wd, moe_w4_t Wd_s, float* Y, void* ws,
                             size_t ws_bytes, void* stream);
+
+/* moe_down_combine_w4a16 -- the down projection with the weighted combine
+ * fused in (the deterministic scatter-add of the same FFAI commit, here a
+ * fixed-order per-token sum instead of atomics):
+ *   out[t] = bf16( [float(residual[t]) +] (sum_j topk_w[t][j] * Y[pos[t*k+j]]
+ *                                           + Y[T*k + t]) ),
+ * the same value and summation order as moe_down_w4a16 followed by
+ * moe_combine_shared (or moe_combine_shared_residual), without the caller's Y.
+ * On the GEMV path (T <= 4 by default) the combine runs inside the down
+ * kernel and Y stays in L2; on the grouped path it is the down launch and a
+ * combine launch, Y in the workspace.
+ *   topk_w   (device) fp32 [T][k], from moe_router_topk
+ *   pos      (device) int32 [T*k], from moe_build_descriptors
+ *   residual (device) bf16 [T][d], 16-byte aligned, or NULL; may be out
+ *   out      (device) out: bf16 [T][d], 16-byte aligned
+ *   ws       a workspace of moe_layer_workspace_bytes(dims), the one
+ *            moe_build_descriptors filled for this batch (Y lives in it)
+ */
+moe_status_t moe_down_combine_w4a16(const uint16_t* H, const moe_dims_t* dims,
+                                    const int32_t* offsets, const int32_t* sched,
+                                    const float* topk_w, const int32_t* pos, moe_w4_t Wd,
+                                    moe_w4_t Wd_s, const uint16_t* residual, uint16_t* out,
+                                    void* ws, size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------------------------
  * moe_combine_shared -- weighted combine of the routed rows plus the shared

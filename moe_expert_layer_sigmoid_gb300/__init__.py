@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_layer_workspace_bytes", "moe_layer_forward", "moe_layer_forward_host",
     "moe_check_device_status", "moe_router_topk_noalloc", "moe_pack_w4_bytes",
     "moe_combine_shared_residual", "moe_layer_forward_residual", "moe_import_q4_blocks",
+    "moe_down_combine_w4a16",
 )
 
 
@@ -86,6 +87,7 @@ def lib() -> ctypes.CDLL:
         "moe_build_descriptors": ([p, D, p, p, p, p, p, p, sz, p], i32),
         "moe_gateup_swiglu_w4a16": ([p, D, p, p, p, W4, W4, p, p, sz, p], i32),
         "moe_down_w4a16": ([p, D, p, p, W4, W4, p, p, sz, p], i32),
+        "moe_down_combine_w4a16": ([p, D, p, p, p, p, W4, W4, p, p, p, sz, p], i32),
         "moe_pack_w4_bytes": ([i64, i64, i32, ctypes.POINTER(sz)], sz),
         "moe_import_q4_blocks": ([p, i64, i64, i32, p, p, p, p], i32),
         "moe_combine_shared": ([p, p, p, D, p, p], i32),
@@ -237,6 +239,19 @@ def moe_down_w4a16(H, dims: Dims, offsets, sched, Wd: W4, Wd_s: W4, Y, ws, strea
         _dev(H, torch.int16, "H"), ctypes.byref(dims), _dev(offsets, torch.int32, "offsets"),
         _dev(sched, torch.int32, "sched"), Wd, Wd_s, _dev(Y, torch.float32, "Y"), _ptr(ws),
         ws.numel(), _stream(stream)), "moe_down_w4a16")
+
+
+def moe_down_combine_w4a16(H, dims: Dims, offsets, sched, topk_w, pos, Wd: W4, Wd_s: W4,
+                           residual, out, ws, stream=None):
+    """Down projection with the weighted combine (and an optional residual) fused in;
+    ws is a layer-sized workspace (it holds Y)."""
+    _check(lib().moe_down_combine_w4a16(
+        _dev(H, torch.int16, "H"), ctypes.byref(dims), _dev(offsets, torch.int32, "offsets"),
+        _dev(sched, torch.int32, "sched"), _dev(topk_w, torch.float32, "topk_w"),
+        _dev(pos, torch.int32, "pos"), Wd, Wd_s,
+        None if residual is None else _dev(residual, torch.int16, "residual"),
+        _dev(out, torch.int16, "out"), _ptr(ws), ws.numel(), _stream(stream)),
+        "moe_down_combine_w4a16")
 
 
 def moe_combine_shared(Y, topk_w, pos, dims: Dims, out, stream=None):

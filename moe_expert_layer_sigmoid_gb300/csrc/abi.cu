@@ -402,6 +402,37 @@ moe_status_t moe_down_w4a16(const uint16_t* H, const moe_dims_t* dims, const int
     return down_impl(H, *dims, offsets, sched, Wd, Wd_s, Y, ws, static_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_down_combine_w4a16(const uint16_t* H, const moe_dims_t* dims,
+                                    const int32_t* offsets, const int32_t* sched,
+                                    const float* topk_w, const int32_t* pos, moe_w4_t Wd,
+                                    moe_w4_t Wd_s, const uint16_t* residual, uint16_t* out,
+                                    void* ws, size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.layer_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!act_ok(H) || !offsets || !sched || !topk_w || !pos || !act_ok(out) || !w4_ok(Wd) ||
+        !w4_ok(Wd_s) || (residual && !act_ok(residual)))
+        return MOE_ERR_INVALID_ARG;
+    const moe_dims_t& d = *dims;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* Y = ws_at<float>(ws, L.Y);
+    WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
+    switch (expert_path(d)) {
+        case Path::kGemv:
+            if ((d.flags & MOE_FLAG_DECODE_MMA) && tc_decode_supported(d) && tc_weights_ok(Wd, Wd_s))
+                return map_err(launch_down_tc(H, d, offsets, sched, Wd, Wd_s, Y, nullptr, topk_w,
+                                              pos, residual, out, false, s));
+            return map_err(launch_down_gemv(H, d, offsets, sched, Wd, Wd_s, Y, nullptr, topk_w, pos,
+                                            residual, out, hdr, false, s));
+        case Path::kGrouped:
+            if ((st = down_impl(H, d, offsets, sched, Wd, Wd_s, Y, ws, s)) != MOE_OK) return st;
+            return map_err(launch_combine(Y, topk_w, pos, d, residual, out, s));
+        default: return MOE_ERR_UNSUPPORTED;
+    }
+}
+
 moe_status_t moe_combine_shared(const float* Y, const float* topk_w, const int32_t* pos,
                                 const moe_dims_t* dims, uint16_t* out, void* stream) {
     moe_status_t st = check_dims(dims);

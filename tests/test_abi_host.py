@@ -191,3 +191,26 @@ def test_import_q4_blocks_validation(L):
     assert L.moe_import_q4_blocks(None, 2, 64, 32, ok, ok, ok, None) == INV
     assert L.moe_import_q4_blocks(ok, 2, 64, 32, ok + 4, ok, ok, None) == INV  # w_scratch align
     assert L.moe_import_q4_blocks(ok, 2, 64, 32, ok, ok + 2, ok, None) == INV  # q align
+
+
+def test_down_combine_validation(L):
+    d = _dims()
+    step, layer = moe.moe_workspace_bytes(d), moe.moe_layer_workspace_bytes(d)
+    ws, ok, bad = 1 << 20, 1 << 21, (1 << 21) + 8
+    w4 = moe.W4(ok, ok)
+    INV = moe.MOE_ERR_INVALID_ARG
+
+    def call(H=ok, topk_w=ok, pos=ok, residual=None, out=ok, nbytes=layer, dims=d):
+        return L.moe_down_combine_w4a16(H, ctypes.byref(dims), ok, ok, topk_w, pos, w4, w4,
+                                        residual, out, ws, nbytes, None)
+
+    assert call(nbytes=step) == moe.MOE_ERR_WORKSPACE  # Y lives in the layer workspace
+    assert call(H=bad) == INV
+    assert call(out=bad) == INV
+    assert call(residual=bad) == INV
+    assert call(topk_w=None) == INV
+    assert call(pos=None) == INV
+    assert call(dims=_dims(group=48)) == moe.MOE_ERR_UNSUPPORTED
+    d0 = _dims(T=0)
+    assert call(H=None, topk_w=None, pos=None, out=None, dims=d0,
+                nbytes=moe.moe_layer_workspace_bytes(d0)) == moe.MOE_OK

@@ -222,6 +222,42 @@ def test_stepwise_calls_match_forward_and_oracle_h(C):
     assert ok
 
 
+@pytest.mark.parametrize("flags", [0, moe.MOE_FLAG_FORCE_GEMV])
+def test_down_combine_matches_down_then_combine(C, flags):
+    """moe_down_combine_w4a16 (the combine fused into the down projection) gives the
+    bits of moe_down_w4a16 followed by moe_combine_shared, and with a residual those of
+    moe_combine_shared_residual."""
+    dev, cfg = C.dev, C.cfg
+    if flags and cfg.T > 64:
+        pytest.skip("the forced GEMV is checked up to the decode sizes")
+    T, k, E, d = cfg.T, cfg.k, cfg.E, cfg.d
+    dims = dev.dims(flags)
+    ws = moe.workspace(moe.moe_layer_workspace_bytes(dims))
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx = torch.empty((T, k), **i32)
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    perm, pos, sched = torch.empty(T * k, **i32), torch.empty(T * k, **i32), torch.empty(E, **i32)
+    H = torch.empty((T * k + T, max(cfg.F, cfg.Fs)), dtype=torch.int16, device="cuda")
+    Y = torch.empty((T * k + T, d), dtype=torch.float32, device="cuda")
+    Wgu, Wd, Wgu_s, Wd_s = dev.w4s()
+    moe.moe_router_topk(dev.x, dev.W_r, dev.bias, dims, idx, w, None, ws)
+    moe.moe_build_descriptors(idx, dims, counts, offsets, perm, pos, sched, ws)
+    moe.moe_gateup_swiglu_w4a16(dev.x, dims, offsets, perm, sched, Wgu, Wgu_s, H, ws)
+    moe.moe_down_w4a16(H, dims, offsets, sched, Wd, Wd_s, Y, ws)
+    ref = torch.empty((T, d), dtype=torch.int16, device="cuda")
+    moe.moe_combine_shared(Y, w, pos, dims, ref)
+    out = torch.empty_like(ref)
+    moe.moe_down_combine_w4a16(H, dims, offsets, sched, w, pos, Wd, Wd_s, None, out, ws)
+    assert moe.moe_check_device_status(ws) == moe.MOE_OK
+    assert torch.equal(out, ref)
+    r = (torch.randn((T, d), device="cuda") * 0.05).to(torch.bfloat16).view(torch.int16)
+    moe.moe_combine_shared_residual(Y, w, pos, dims, r, ref)
+    moe.moe_down_combine_w4a16(H, dims, offsets, sched, w, pos, Wd, Wd_s, r, out, ws)
+    assert moe.moe_check_device_status(ws) == moe.MOE_OK
+    assert torch.equal(out, ref)
+
+
 def test_forced_paths_agree(C):
     """The decode GEMV and the grouped path compute the same layer."""
     if C.cfg.T > 2048:
