@@ -358,6 +358,21 @@ def test_identity_like_experts_closed_form(oracle_lib):
         assert np.array_equal(res["out"][t], expect_bits), t
 
 
+def test_closed_form_layer_of_the_gpu_tests_on_the_oracle(oracle_lib):
+    """The GPU suite's larger identity-like layer (alternating up-row signs, overlapping
+    coordinate sets, group 32) gives the closed form bit for bit on the oracle too."""
+    from closed_form import (CF, CF_CHOSEN, bf16_bits, closed_form_expect, closed_form_inputs,
+                             closed_form_weights)
+    coords, sign, Wgu, Wd, Wgu_s, Wd_s = closed_form_weights(31)
+    W = _pack_expert_stack(oracle_lib, Wgu, Wd, Wgu_s, Wd_s, CF["group"])
+    x = closed_form_inputs(5, 32)
+    b = np.zeros(CF["E"], np.float32)
+    b[list(CF_CHOSEN)] = 10.0
+    res = oracle_lib.layer(bf16_bits(x), np.zeros((CF["E"], CF["d"]), np.float32), b, W, CF["k"])
+    assert np.all(np.sort(res["topk_idx"], 1) == list(CF_CHOSEN))
+    assert np.array_equal(res["out"], closed_form_expect(x, coords, sign))
+
+
 def _random_layer(oracle_lib, T=6, d=64, E=8, k=3, F=32, Fs=32, group=16, seed=0):
     rng = np.random.default_rng(seed)
     x = torch.from_numpy(rng.standard_normal((T, d)).astype(np.float32)).to(torch.bfloat16)
