@@ -5,7 +5,15 @@ SwiGLU, down projection, combine with the shared expert) over one batch of
 synthetic tokens, through the C ABI (moe_layer_forward), replayed as a CUDA
 graph.  The headline workload is single-token decode (T = 1, d 4096, 256
 experts, top-10, FFN 1024 + shared 1024, int4 g128); the same JSON line also
-carries the T = 2048 chunked-prefill pass under "secondary".
+carries, under "secondary", the 32-token decode batch, the T = 2048
+chunked-prefill pass and the T = 8192 skewed-routing pass (the latter also
+with the grouped kernel's CTA scheduling switched off, MOE_FLAG_NO_SCHED).
+
+Timing: the --steps steps of a config are one window, bracketed by a
+synchronize (and a barrier across ranks) and timed with CUDA events on the
+launching stream; windows are repeated (at least 5, and for at least a
+second so that the clock sampler sees the load) and the median window is
+reported.
 
 Inputs larger than L2: each step reads a different copy of the packed
 weights (NCOPY copies, each 1.67 GB) and a different activation batch, so
@@ -33,7 +41,12 @@ if ROOT not in sys.path:
 import workloads  # noqa: E402
 
 HEADLINE = "decode1"
-SECONDARY = "prefill2048"
+SECONDARY = "decode32,prefill2048,skew8192"
+# steps per timed window of each secondary config (about 0.1-0.5 s each)
+SECONDARY_STEPS = {"decode1": 4000, "decode32": 1000, "prefill2048": 300, "skew8192": 60,
+                   "tiny": 4000}
+MIN_WINDOWS = 5
+MIN_TIMED_S = 1.0  # default of --min-time
 METRIC = "MoE-layer tokens/s at T=1 and T=2048; % of HBM / BF16 tensor-core roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -113,6 +126,8 @@ class ClockSampler:
 def kernels_per_step(cfg, flags=0):
     """Kernels libmoe.so launches for one moe_layer_forward (memset nodes excluded)."""
     gemv = (flags & 0x1) or (cfg.T <= 4 and not flags & 0x2)
+    if gemv and cfg.T == 1 and flags & 0x8:
+        return 1  # the cooperative single-launch step
     if gemv and cfg.T <= 64:
         return 3  # fused router + descriptors, gate+up GEMV, down GEMV + combine
     if gemv:
@@ -133,15 +148,18 @@ class GpuBench:
         self.layer = upload(cfg, device=device, extra_batches=nbatch - 1)
         L = self.layer
         self.xs = [L.x] + list(L.x_batches)
-        # weight copies: copy 0 is the uploaded one
+        # weight copies: copy 0 is the uploaded one; every copy has its own router
+        # weights too, as every layer of a model does, so none stays in L2
         self.copies = [L.w4s()]
+        self.routers = [(L.W_r, L.bias)]
         self._keep = []
         for _ in range(ncopy - 1):
             ts = [t.clone() for t in (L.gu_q, L.gu_s, L.dn_q, L.dn_s, L.sgu_q, L.sgu_s, L.sdn_q,
-                                      L.sdn_s)]
+                                      L.sdn_s, L.W_r, L.bias)]
             self._keep.append(ts)
             self.copies.append((moe.w4(ts[0], ts[1]), moe.w4(ts[2], ts[3]), moe.w4(ts[4], ts[5]),
                                 moe.w4(ts[6], ts[7])))
+            self.routers.append((ts[8], ts[9]))
         self.dims = L.dims()
         self.dims.flags = flags
         self.ws = moe.workspace(moe.moe_layer_workspace_bytes(self.dims), device)
@@ -151,9 +169,9 @@ class GpuBench:
 
     def step(self, i, stream=None):
         c = self.copies[i % len(self.copies)]
+        wr, bias = self.routers[i % len(self.routers)]
         x = self.xs[i % len(self.xs)]
-        self.moe.moe_layer_forward(x, self.layer.W_r, self.layer.bias, self.dims, *c, self.out,
-                                   self.ws, stream=stream)
+        self.moe.moe_layer_forward(x, wr, bias, self.dims, *c, self.out, self.ws, stream=stream)
 
     def capture(self):
         """One graph per slot, and one graph of all slots in a row (so that a
@@ -183,19 +201,56 @@ class GpuBench:
         for i in range(rest):
             self.graphs[i].replay()
 
-    def run(self, warmup: int, steps: int):
+    def run(self, warmup: int, steps: int, clocks=None, min_time: float = MIN_TIMED_S):
+        """Median ms per step over repeated windows of exactly `steps` steps (at least
+        MIN_WINDOWS windows and MIN_TIMED_S seconds); the clock sampler runs across all
+        windows.  Returns (median, per-window list)."""
         torch = self.torch
         with torch.cuda.stream(self.stream):
             self.replay_steps(warmup)
         torch.cuda.synchronize(self.device)
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(self.stream):
-            start.record(self.stream)
-            self.replay_steps(steps)
-            end.record(self.stream)
-        end.synchronize()
-        return start.elapsed_time(end) / steps  # ms per step
+        if clocks is not None:
+            clocks.start()
+        per = []
+
+        def window():
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(self.device)
+            barrier()
+            with torch.cuda.stream(self.stream):
+                start.record(self.stream)
+                self.replay_steps(steps)
+                end.record(self.stream)
+            end.synchronize()
+            barrier()
+            per.append(start.elapsed_time(end) / steps)
+
+        window()
+        # the same number of windows on every rank (each window is a barrier pair)
+        n = max(MIN_WINDOWS, int(np.ceil(min_time / max(per[0] * steps * 1e-3, 1e-6))))
+        n = int(max_over_ranks(float(min(n, 100000)), self.device))
+        while len(per) < n:
+            window()
+        clk = clocks.stop() if clocks is not None else None
+        return float(np.median(per)), per, clk
+
+    def windows(self, enqueue, units: int, min_windows: int = MIN_WINDOWS):
+        """Median ms per unit over at least min_windows CUDA-event windows, each running
+        enqueue() (which issues `units` units of work) on the bench stream."""
+        torch = self.torch
+        per = []
+        for _ in range(min_windows):
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(self.device)
+            with torch.cuda.stream(self.stream):
+                start.record(self.stream)
+                enqueue()
+                end.record(self.stream)
+            end.synchronize()
+            per.append(start.elapsed_time(end) / units)
+        return float(np.median(per))
 
     def descriptors(self, i):
         """Per-slot counts (read back outside any timed region)."""
@@ -244,16 +299,15 @@ class GpuBench:
         with torch.cuda.stream(self.stream):
             for _ in range(reps_w):
                 g.replay()
-            self.stream.synchronize()
-            start = torch.cuda.Event(enable_timing=True)
-            end = torch.cuda.Event(enable_timing=True)
-            start.record(self.stream)
+        self.stream.synchronize()
+
+        def enqueue():
             for _ in range(reps):
                 g.replay()
-            end.record(self.stream)
-        end.synchronize()
+
+        ms = self.windows(enqueue, reps * self.nslots)
         active = [int((d["counts"] > 0).sum().item()) for d in descs]
-        return start.elapsed_time(end) / (reps * self.nslots), active
+        return ms, active
 
     def e2e(self, warmup: int, steps: int):
         """moe_layer_forward_host: pinned host x in, pinned host out, captured as a graph."""
@@ -265,8 +319,9 @@ class GpuBench:
         oh = torch.empty((T, d), dtype=torch.int16, pin_memory=True)
         def fwd(i):
             c = self.copies[i % len(self.copies)]
-            moe.moe_layer_forward_host(xh[i % len(xh)], self.layer.W_r, self.layer.bias,
-                                       self.dims, *c, oh, self.ws, stream=self.stream)
+            wr, bias = self.routers[i % len(self.routers)]
+            moe.moe_layer_forward_host(xh[i % len(xh)], wr, bias, self.dims, *c, oh, self.ws,
+                                       stream=self.stream)
 
         graphs = []
         for i in range(self.nslots):
@@ -292,14 +347,7 @@ class GpuBench:
         with torch.cuda.stream(self.stream):
             replay(warmup)
         torch.cuda.synchronize(self.device)
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(self.stream):
-            start.record(self.stream)
-            replay(steps)
-            end.record(self.stream)
-        end.synchronize()
-        ms = start.elapsed_time(end) / steps
+        ms = self.windows(lambda: replay(steps), steps)
         return ms, 2 * T * d, 2 * T * d
 
     def free(self):
@@ -312,12 +360,10 @@ class GpuBench:
 
 
 # DRAM bytes (read + write) per step of the decode chain at decode1, summed over
-# router_decode_kernel, gateup_gemv_kernel and down_gemv_kernel from one
-# `ncu --set full` capture of each (cold caches).  down_gemv_kernel has changed
-# since (its combine takes an optional residual pointer), so the line reports
-# traffic as null and this figure as the prior capture until it is re-taken.
-DECODE1_TRAFFIC = 4_269_312 + 48_279_552 + 27_392 + 23_851_264
-DECODE1_TRAFFIC_CURRENT = False
+# router_decode_kernel, gateup_gemv_kernel and down_gemv_kernel of one step, from
+# one `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` capture of this
+# code (cold caches, --ncopy 1 --nbatch 1, one step of three launches).
+DECODE1_TRAFFIC = 4_269_312 + 48_285_696 + 23_853_824
 
 
 def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
@@ -330,16 +376,15 @@ def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
     achieved = nbytes / (ms * 1e-3) / 1e9
     peak = pk["hbm_gbs"]
     router_bytes = cfg.E * cfg.d * 4
+    kernel_of_step = kernels_per_step(cfg, flags)
     kernel = ("decode step: router_decode_kernel + gateup_gemv_kernel + down_gemv_kernel"
-              if kernels_per_step(cfg, flags) == 3 else
+              if kernel_of_step == 3 else
               "layer step on the grouped path (router, descriptors, gather, grouped GEMMs, combine)")
     return {"kernel": kernel,
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": (DECODE1_TRAFFIC if cfg.name == "decode1" and DECODE1_TRAFFIC_CURRENT
+            "traffic": (DECODE1_TRAFFIC if cfg.name == "decode1" and kernel_of_step == 3
                         else None),
-            **({"traffic_prior_capture": DECODE1_TRAFFIC}
-               if cfg.name == "decode1" and not DECODE1_TRAFFIC_CURRENT else {}),
             "bytes_per_step": int(nbytes),
             "router_weight_bytes_not_counted": router_bytes,
             "step_us": round(ms * 1e3, 3),
@@ -365,20 +410,27 @@ def gpu_roofline_prefill(cfg, gu_ms, pk, pk_kind):
             "peak_source": f"{pk_kind} bf16_tflops"}
 
 
-def measure_config(name, device, warmup, steps, ncopy, nbatch, pk, pk_kind, gpu_index, flags=0):
+def measure_config(name, device, warmup, steps, ncopy, nbatch, pk, pk_kind, gpu_index, flags=0,
+                   ab_flags=None, min_time=MIN_TIMED_S):
+    """Layer step (median of windows, clocks sampled across them), the standalone gate+up
+    launch, and the end-to-end host call, on one config.  With ab_flags, the layer step
+    and the gate+up launch are timed again with those flags (same inputs)."""
     cfg = workloads.CONFIGS[name]
     b = GpuBench(cfg, device, ncopy=ncopy, nbatch=nbatch, flags=flags)
     b.capture()
-    clocks = ClockSampler(gpu_index)
-    clocks.start()
-    ms = b.run(warmup, steps)
-    clk = clocks.stop()
+    ms, per, clk = b.run(warmup, steps, ClockSampler(gpu_index), min_time)
     gu_ms, active = b.time_gateup(warmup, steps)
     e2e_ms, h2d, d2h = b.e2e(warmup, steps)
     layer_bytes = float(np.mean([(a + 1) * cfg.packed_expert_bytes() for a in active]))
-    res = dict(cfg=cfg, ms=ms, clocks=clk, gu_ms=gu_ms, active=active, e2e_ms=e2e_ms, h2d=h2d,
-               d2h=d2h, layer_bytes=layer_bytes, packed_copies=len(b.copies),
-               batches=len(b.xs))
+    res = dict(cfg=cfg, ms=ms, windows=per, clocks=clk, gu_ms=gu_ms, active=active,
+               e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, layer_bytes=layer_bytes,
+               packed_copies=len(b.copies), batches=len(b.xs), steps=steps, flags=flags)
+    if ab_flags is not None:
+        b.dims.flags = ab_flags
+        b.capture()
+        ms_ab, per_ab, clk_ab = b.run(warmup, steps, ClockSampler(gpu_index), min_time)
+        gu_ab, _ = b.time_gateup(warmup, steps)
+        res["ab"] = dict(flags=ab_flags, ms=ms_ab, windows=per_ab, clocks=clk_ab, gu_ms=gu_ab)
     b.free()
     return res
 
@@ -424,6 +476,13 @@ def oracle_sample(cfg, budget_s: float, max_tokens: int):
 
 # ---------------------------------------------------------------- main
 
+def barrier():
+    """A barrier across ranks when a process group is up."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
 def max_over_ranks(x: float, device="cpu") -> float:
     """The largest of a per-rank value over the process group (the slowest rank's step time
     sets the job's throughput); the value itself when no group is initialised."""
@@ -441,6 +500,75 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def config_dict(cfg, ncopy: int, nbatch: int) -> dict:
+    """The workload, worded identically in both arms."""
+    return {
+        "workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, top-{cfg.k}, F={cfg.F}, "
+                    f"shared F={cfg.Fs}, int4 g{cfg.group}, seed {cfg.seed}",
+        "l2": f"inputs larger than L2: {ncopy} copies of the expert and router weights x "
+              f"{nbatch} activation batches, rotated per step",
+    }
+
+
+def timing_dict(res) -> dict:
+    w = res["windows"]
+    return {"method": "CUDA graph replay of moe_layer_forward; CUDA events on the launching "
+                      "stream around each window of --steps steps; median window reported",
+            "windows": len(w), "steps_per_window": res["steps"],
+            "ms_per_step_min": round(min(w), 5), "ms_per_step_max": round(max(w), 5)}
+
+
+def e2e_dict(res) -> dict:
+    cfg = res["cfg"]
+    return {"value": round(cfg.T / (res["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+            "ms_per_step": round(res["e2e_ms"], 5),
+            "mode": "graph replay of moe_layer_forward_host (pinned host x and out), "
+                    "median of 5 windows"}
+
+
+def roofline_of(res, ms, pk, pk_kind) -> dict:
+    cfg = res["cfg"]
+    if cfg.T <= 64:  # decode: weight streaming against HBM, per step
+        return gpu_roofline_decode(cfg, ms, res["active"], pk, pk_kind, res["gu_ms"],
+                                   res["flags"])
+    # prefill: the gate+up grouped kernel against the dense bf16 peak
+    roof = gpu_roofline_prefill(cfg, res["gu_ms"], pk, pk_kind)
+    roof["layer_tflops"] = round(cfg.flops() / (ms * 1e-3) / 1e12, 2)
+    roof["layer_frac_of_bf16_peak"] = round(roof["layer_tflops"] / pk["bf16_tflops"], 4)
+    return roof
+
+
+def secondary_entry(res, pk, pk_kind) -> dict:
+    cfg = res["cfg"]
+    ms = res["ms"]
+    tf = cfg.flops() / (ms * 1e-3) / 1e12
+    ent = {
+        "workload": config_dict(cfg, res["packed_copies"], res["batches"])["workload"],
+        "value": round(cfg.T / (ms * 1e-3), 1), "unit": "tokens/s",
+        "us_per_layer": round(ms * 1e3, 2),
+        "layer_tflops": round(tf, 2),
+        "layer_frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+        "active_experts_mean": float(np.mean(res["active"])),
+        "kernels_per_step": kernels_per_step(cfg, res["flags"]),
+        "timing": timing_dict(res),
+        "roofline": roofline_of(res, ms, pk, pk_kind),
+        "clocks": res["clocks"],
+        "e2e": e2e_dict(res),
+    }
+    if "ab" in res:
+        ab = res["ab"]
+        ent["no_sched"] = {
+            "flags": "MOE_FLAG_NO_SCHED (expert-id tile order, no N-banding)",
+            "us_per_layer": round(ab["ms"] * 1e3, 2),
+            "gateup_us": round(ab["gu_ms"] * 1e3, 2),
+            "windows": len(ab["windows"]), "clocks": ab["clocks"],
+            "sched_speedup_layer": round(ab["ms"] / ms, 4),
+            "sched_speedup_gateup": round(ab["gu_ms"] / res["gu_ms"], 4),
+        }
+    return ent
 
 
 REF_BUDGET_S = 120.0  # cap on the reference arm's timed oracle work
@@ -462,9 +590,9 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec / n * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 (fp64 router)", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, top-{cfg.k}, "
-                               f"F={cfg.F}, shared F={cfg.Fs}, int4 g{cfg.group}",
-                   "step": "one token of the workload through the oracle"},
+        "config": config_dict(cfg, args.ncopy, args.nbatch),
+        "step": "one token of the workload through the oracle",
+        "parallelism": "rank 0 only, one host thread",
         "steps_timed": n,
         "cpu_baseline": {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{n} tokens of {cfg.name}, one per step, single thread "
@@ -483,11 +611,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=HEADLINE, choices=sorted(workloads.CONFIGS))
-    ap.add_argument("--secondary", default=SECONDARY, help="extra config in the same line ('' = none)")
-    ap.add_argument("--secondary-steps", type=int, default=400)
+    ap.add_argument("--secondary", default=SECONDARY,
+                    help="comma-separated extra configs in the same line ('none': no extra config)")
+    ap.add_argument("--secondary-steps", type=int, default=0,
+                    help="steps per timed window of each extra config (0: a per-config default)")
     ap.add_argument("--ncopy", type=int, default=8)
     ap.add_argument("--nbatch", type=int, default=8)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--min-time", type=float, default=MIN_TIMED_S,
+                    help="repeat timed windows for at least this many seconds (>= 5 windows)")
     ap.add_argument("--flags", type=int, default=0,
                     help="moe_dims_t.flags for the headline config (1: force GEMV, 2: force grouped)")
     args = ap.parse_args()
@@ -510,11 +642,18 @@ def main():
     if world > 1:
         dist.barrier()
     main_res = measure_config(args.config, device, args.warmup, args.steps, args.ncopy,
-                              args.nbatch, pk, pk_kind, gpu_index, flags=args.flags)
-    sec_res = None
-    if args.secondary and args.secondary != args.config:
-        sec_res = measure_config(args.secondary, device, args.warmup, args.secondary_steps,
-                                 args.ncopy, args.nbatch, pk, pk_kind, gpu_index)
+                              args.nbatch, pk, pk_kind, gpu_index, flags=args.flags,
+                              min_time=args.min_time)
+    sec_names = [] if args.secondary in ("", "none", '""') else \
+        [n for n in args.secondary.split(",") if n and n != args.config]
+    sec_res = []
+    for name in sec_names:
+        steps = args.secondary_steps or SECONDARY_STEPS.get(name, 100)
+        # the skewed config also runs without the grouped kernel's CTA scheduling
+        ab = 0x4 if workloads.CONFIGS[name].bias == "zipf" else None
+        sec_res.append(measure_config(name, device, args.warmup, steps, args.ncopy, args.nbatch,
+                                      pk, pk_kind, gpu_index, ab_flags=ab,
+                                      min_time=args.min_time))
     ms = max_over_ranks(main_res["ms"], device)
     cfg = main_res["cfg"]
     value = world * cfg.T / (ms * 1e-3)
@@ -527,56 +666,27 @@ def main():
                          f"{sec:.1f} s of single-thread CPU work"}
 
     if rank == 0:
-        if cfg.T <= 64:  # decode: weight streaming against HBM, per step
-            roof = gpu_roofline_decode(cfg, ms, main_res["active"], pk, pk_kind, main_res["gu_ms"],
-                                       args.flags)
-        else:  # prefill: the gate+up grouped kernel against the dense bf16 peak
-            roof = gpu_roofline_prefill(cfg, main_res["gu_ms"], pk, pk_kind)
-            roof["layer_tflops"] = round(cfg.flops() / (ms * 1e-3) / 1e12, 2)
-            roof["layer_frac_of_bf16_peak"] = round(roof["layer_tflops"] / pk["bf16_tflops"], 4)
+        roof = roofline_of(main_res, ms, pk, pk_kind)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "us_per_layer": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int4 weights x bf16 activations, f32 accumulate",
             "data": "synthetic (seeded generator, random weights of the layer's shapes)",
-            "config": {
-                "workload": f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, top-{cfg.k}, F={cfg.F}, "
-                            f"shared F={cfg.Fs}, int4 g{cfg.group}, seed {cfg.seed}",
-                "l2": f"inputs larger than L2: {main_res['packed_copies']} weight copies x "
-                      f"{main_res['batches']} activation batches rotated per step",
-                "timing": "CUDA graph replay of moe_layer_forward, CUDA events over the timed steps",
-                "parallelism": "replicas" if world > 1 else "single GPU",
-            },
+            "config": config_dict(cfg, args.ncopy, args.nbatch),
+            "parallelism": f"{world} replicas, no collective" if world > 1 else "single GPU",
+            "timing": timing_dict(main_res),
             "roofline": roof,
             "active_experts_mean": float(np.mean(main_res["active"])),
             "clocks": main_res["clocks"],
-            "e2e": {"value": round(cfg.T / (main_res["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
-                    "h2d_bytes_per_step": main_res["h2d"], "d2h_bytes_per_step": main_res["d2h"],
-                    "ms_per_step": round(main_res["e2e_ms"], 5),
-                    "mode": "graph replay of moe_layer_forward_host (pinned host x and out)"},
+            "e2e": e2e_dict(main_res),
             "gpu_launches": kernels_per_step(cfg, args.flags) * args.steps,
             "kernels_per_step": kernels_per_step(cfg, args.flags),
             "cpu_baseline": cpu,
             "peaks": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback",
         }
-        if sec_res is not None:
-            scfg = sec_res["cfg"]
-            sroof = (gpu_roofline_prefill(scfg, sec_res["gu_ms"], pk, pk_kind) if scfg.T > 64 else
-                     gpu_roofline_decode(scfg, sec_res["ms"], sec_res["active"], pk, pk_kind,
-                                         sec_res["gu_ms"]))
-            tf = scfg.flops() / (sec_res["ms"] * 1e-3) / 1e12
-            line["secondary"] = {
-                "workload": f"{scfg.name}: T={scfg.T}, same layer shapes, seed {scfg.seed}",
-                "value": round(scfg.T / (sec_res["ms"] * 1e-3), 1), "unit": "tokens/s",
-                "us_per_layer": round(sec_res["ms"] * 1e3, 1),
-                "layer_tflops": round(tf, 2),
-                "layer_frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
-                "roofline": sroof, "clocks": sec_res["clocks"],
-                "e2e": {"value": round(scfg.T / (sec_res["e2e_ms"] * 1e-3), 1),
-                        "unit": "tokens/s", "h2d_bytes_per_step": sec_res["h2d"],
-                        "d2h_bytes_per_step": sec_res["d2h"]},
-            }
+        if sec_res:
+            line["secondary"] = [secondary_entry(r, pk, pk_kind) for r in sec_res]
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

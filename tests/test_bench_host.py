@@ -54,7 +54,7 @@ def test_reference_arm_is_bounded_in_time(monkeypatch):
     monkeypatch.setattr(bench, "oracle_sample", fake_sample)
 
     class A:
-        config, steps, warmup = "decode1", 40000, 10
+        config, steps, warmup, ncopy, nbatch = "decode1", 40000, 10, 8, 8
 
     assert bench.run_reference(A) == 0
     assert calls[-1] == (bench.REF_BUDGET_S, 40000) and bench.REF_BUDGET_S <= 180
@@ -71,9 +71,17 @@ def test_reference_arm_other_ranks_exit_quietly():
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
+def test_reference_config_is_the_gpu_arms_config():
+    """Both arms word the workload with the same function and the same defaults."""
+    r = _run("--impl", "reference", "--steps", "1", "--warmup", "3")
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["config"] == bench.config_dict(workloads.CONFIGS["decode1"], 8, 8)
+    assert "seed 1" in d["config"]["workload"]
+
+
 @pytest.mark.parametrize("name,flags,n", [("decode1", 0, 3), ("tiny", 0, 3), ("decode32", 0, 10),
                                           ("prefill2048", 0, 10), ("decode32", 1, 3),
-                                          ("decode1", 2, 10)])
+                                          ("decode1", 2, 10), ("decode1", 8, 1)])
 def test_kernels_per_step(name, flags, n):
     assert bench.kernels_per_step(workloads.CONFIGS[name], flags) == n
 
