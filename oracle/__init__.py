@@ -66,6 +66,13 @@ def _get():
         "orc_f32_to_bf16_array": [p, i64, p],
         "orc_f64_to_bf16_array": [p, i64, p],
         "orc_bf16_to_f32_array": [p, i64, p],
+        "orc_pack_w8": [p, i64, i64, p, p],
+        "orc_quant_rows_fp8": [p, i64, i64, p, p],
+        "orc_expert_token_w8a8": [p, i32, i32, p, p, p, p, p, p],
+        "orc_layer_w8a8_tokens": [p, i32, i32, i32, i32, p, p, p, p, p, p, p, p, p, p, p, i64,
+                                  p, p, p],
+        "orc_f32_to_e4m3_array": [p, i64, p],
+        "orc_e4m3_to_f32_array": [p, i64, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -341,3 +348,134 @@ def layer(x, W_r, bias, W: PackedLayer, k: int, threads: int = 1, want_h: bool =
                                  residual=residual)
     return dict(topk_idx=idx, topk_w=w, margin=margin, out=out, h_routed=h_r, h_shared=h_s,
                 **desc)
+
+
+# ---------------------------------------------------------------- W8A8 (fp8 E4M3)
+
+def f32_to_e4m3(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _get().orc_f32_to_e4m3_array(_p(x), x.size, _p(out))
+    return out
+
+
+def e4m3_to_f32(b) -> np.ndarray:
+    b = np.ascontiguousarray(b, np.uint8)
+    out = np.empty(b.shape, np.float32)
+    _get().orc_e4m3_to_f32_array(_p(b), b.size, _p(out))
+    return out
+
+
+def pack_w8(w):
+    """w fp32 [rows][K] -> (q E4M3 codes uint8 [rows][K], s fp32 [rows])."""
+    w = np.ascontiguousarray(w, np.float32)
+    rows, K = w.shape
+    q = np.empty((rows, K), np.uint8)
+    s = np.empty(rows, np.float32)
+    _get().orc_pack_w8(_p(w), rows, K, _p(q), _p(s))
+    return q, s
+
+
+def quant_rows_fp8(x):
+    """x fp32 [n][K] (activation values) -> (codes uint8 [n][K], a fp32 [n])."""
+    x = np.ascontiguousarray(x, np.float32)
+    n, K = x.shape
+    q = np.empty((n, K), np.uint8)
+    a = np.empty(n, np.float32)
+    _get().orc_quant_rows_fp8(_p(x), n, K, _p(q), _p(a))
+    return q, a
+
+
+def expert_token_w8a8(x_row, q_gu, s_gu, q_dn, s_dn):
+    """One W8A8 expert on one token: returns (h bf16 bits [F], y fp32 [d])."""
+    x_row = np.ascontiguousarray(x_row, np.uint16)
+    d = x_row.shape[0]
+    F = q_gu.shape[0] // 2
+    h = np.empty(F, np.uint16)
+    y = np.empty(d, np.float32)
+    _get().orc_expert_token_w8a8(_p(x_row), d, F, _p(np.ascontiguousarray(q_gu)),
+                                 _p(np.ascontiguousarray(s_gu, np.float32)),
+                                 _p(np.ascontiguousarray(q_dn)),
+                                 _p(np.ascontiguousarray(s_dn, np.float32)), _p(h), _p(y))
+    return h, y
+
+
+class PackedLayerW8:
+    """Oracle-packed W8A8 weights of one layer: codes [E][2F][d], [E][d][F] and the
+    shared expert's [2Fs][d], [d][Fs], with one fp32 scale per row."""
+
+    def __init__(self, q_gu, s_gu, q_dn, s_dn, qs_gu, ss_gu, qs_dn, ss_dn):
+        self.q_gu, self.s_gu, self.q_dn, self.s_dn = q_gu, s_gu, q_dn, s_dn
+        self.qs_gu, self.ss_gu, self.qs_dn, self.ss_dn = qs_gu, ss_gu, qs_dn, ss_dn
+        self.E, twoF, self.d = q_gu.shape
+        self.F = twoF // 2
+        self.Fs = qs_gu.shape[0] // 2
+
+    @staticmethod
+    def from_generator(make_gu, make_dn, E, F, Fs, d, threads: int = 1) -> "PackedLayerW8":
+        """Build from per-expert fp32 producers (expert -1 = shared)."""
+        q_gu = np.empty((E, 2 * F, d), np.uint8)
+        s_gu = np.empty((E, 2 * F), np.float32)
+        q_dn = np.empty((E, d, F), np.uint8)
+        s_dn = np.empty((E, d), np.float32)
+
+        def one(e):
+            q_gu[e], s_gu[e] = pack_w8(make_gu(e))
+            q_dn[e], s_dn[e] = pack_w8(make_dn(e))
+
+        _map(one, range(E), threads)
+        qs_gu, ss_gu = pack_w8(make_gu(-1))
+        qs_dn, ss_dn = pack_w8(make_dn(-1))
+        return PackedLayerW8(q_gu, s_gu, q_dn, s_dn, qs_gu, ss_gu, qs_dn, ss_dn)
+
+    @staticmethod
+    def from_float(Wgu, Wd, Wgu_s, Wd_s, threads: int = 1) -> "PackedLayerW8":
+        E, twoF, d = Wgu.shape
+        return PackedLayerW8.from_generator(lambda e: Wgu[e] if e >= 0 else Wgu_s,
+                                            lambda e: Wd[e] if e >= 0 else Wd_s,
+                                            E, twoF // 2, Wgu_s.shape[0] // 2, d, threads)
+
+
+def layer_w8a8_tokens(x, W: PackedLayerW8, topk_idx, topk_w, tokens, threads: int = 1,
+                      want_h: bool = False):
+    """W8A8 layer output for the listed tokens: (out bf16 bits [n][d], h_routed, h_shared)."""
+    x = np.ascontiguousarray(x, np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, np.int32)
+    topk_w = np.ascontiguousarray(topk_w, np.float32)
+    tokens = np.ascontiguousarray(tokens, np.int64)
+    n = tokens.shape[0]
+    T, d = x.shape
+    k = topk_idx.shape[1]
+    out = np.empty((n, d), np.uint16)
+    h_r = np.empty((n, k, W.F), np.uint16) if want_h else None
+    h_s = np.empty((n, W.Fs), np.uint16) if want_h else None
+    lib = _get()
+
+    def run(a, b):
+        if b <= a:
+            return
+        lib.orc_layer_w8a8_tokens(
+            _p(x), d, k, W.F, W.Fs, _p(topk_idx), _p(topk_w),
+            _p(W.q_gu), _p(W.s_gu), _p(W.q_dn), _p(W.s_dn),
+            _p(W.qs_gu), _p(W.ss_gu), _p(W.qs_dn), _p(W.ss_dn),
+            tokens.ctypes.data + a * 8, b - a, out.ctypes.data + a * d * 2,
+            None if h_r is None else h_r.ctypes.data + a * k * W.F * 2,
+            None if h_s is None else h_s.ctypes.data + a * W.Fs * 2)
+
+    nt = _threads(threads)
+    if nt == 1 or n < 2:
+        run(0, n)
+    else:
+        b = np.linspace(0, n, min(nt, n) + 1).astype(np.int64)
+        with ThreadPoolExecutor(len(b) - 1) as ex:
+            list(ex.map(lambda ab: run(int(ab[0]), int(ab[1])), zip(b[:-1], b[1:])))
+    return out, h_r, h_s
+
+
+def layer_w8a8(x, W_r, bias, W: PackedLayerW8, k: int, threads: int = 1, want_h: bool = False):
+    """The whole W8A8 layer on every token (the router and descriptors are the W4A16
+    layer's)."""
+    idx, w, margin, _ = router(x, W_r, bias, k, threads=threads)
+    out, h_r, h_s = layer_w8a8_tokens(x, W, idx, w, np.arange(x.shape[0]), threads=threads,
+                                      want_h=want_h)
+    return dict(topk_idx=idx, topk_w=w, margin=margin, out=out, h_routed=h_r, h_shared=h_s)

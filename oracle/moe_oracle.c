@@ -54,6 +54,20 @@
  *      s = d (its fp16 bits) and q = n - 8, which is already in [-8, 7].  A
  *      group of 64 or 128 spans blocks with different scales: those rows are
  *      decoded exactly (fp32 holds every (n - 8) * d) and packed with R1-R3.
+ *  R16 W8A8 variant (thewafflehaus/FFAI PR #72, Nemotron-H section: W8A8
+ *      grouped MoE, fp8 activations x fp8 weights; the scale recipe of the
+ *      same pages' FP8 projection commit: one weight scale per output
+ *      channel, one activation scale per token row, both folded in after the
+ *      GEMM).  fp8 is E4M3 without infinities: 1 sign, 4 exponent bits (bias
+ *      7), 3 fraction bits, subnormals down to 2^-9, largest finite 448;
+ *      values round to nearest, ties to even, and saturate to +-448.  A
+ *      weight row w gets s_w = absmax / 448 and q = e4m3(w / s_w); an
+ *      activation row x (the token's bf16 x for gate+up, the bf16 H row for
+ *      down) gets a = absmax / 448 and x_q = e4m3(x / a); both divisions in
+ *      fp32; an all-zero row has scale 0 and codes 0.  A projection is
+ *      v = (acc * a) * s_w, acc = sum_k q_k * x_q,k in fp32 in ascending k
+ *      (every product exact).  SwiGLU, rounding points, combine and shared
+ *      expert as R4-R7 (the shared expert is W8A8 too).
  *  R14 residual add (thewafflehaus/FFAI PR #72, Nemotron commit "ffai_add3":
  *      residual + routed + shared in one launch, routed and shared summed
  *      first): with a residual row r (bf16), out = bf16(float(r) + acc), where
@@ -390,6 +404,137 @@ void orc_layer_tokens(const uint16_t* x, int32_t d, int32_t E, int32_t k, int32_
     free(y);
     free(acc);
     free(h);
+}
+
+/* ------------------------------------------------------------------ */
+/* W8A8 (R16): E4M3 codes, per-row scales, scales folded after the sum.  */
+
+/* E4M3 without infinities, from its definition: value of a code. */
+float orc_e4m3_to_f32(uint8_t b) {
+    int neg = (b >> 7) & 1;
+    int ef = (b >> 3) & 15, frac = b & 7;
+    double v;
+    if (ef == 15 && frac == 7) return NAN;
+    if (ef == 0) v = (double)frac * ldexp(1.0, -9);
+    else v = (1.0 + frac / 8.0) * ldexp(1.0, ef - 7);
+    return (float)(neg ? -v : v);
+}
+
+/* Nearest E4M3 value of x, ties to even, saturating to +-448. */
+uint8_t orc_f32_to_e4m3(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint8_t)(sign | 0x7E);
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1;
+    if (e < -6) e = -6;                         /* subnormal binade shares 2^-6's quantum */
+    double quantum = ldexp(1.0, e - 3);
+    double r = rint(a / quantum) * quantum;
+    if (r > 448.0) r = 448.0;
+    if (r == 0.0) return sign;
+    frexp(r, &ex);
+    e = ex - 1;
+    if (e < -6) return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    return (uint8_t)(sign | ((e + 7) << 3) | (int)((r / ldexp(1.0, e) - 1.0) * 8.0));
+}
+
+/* One row's scale (absmax / 448 in fp32) and codes. */
+static void quant_row_fp8(const float* v, int64_t K, uint8_t* q, float* scale) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < K; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+    float sc = amax / 448.0f;
+    *scale = sc;
+    for (int64_t i = 0; i < K; ++i) q[i] = sc == 0.0f ? 0 : orc_f32_to_e4m3(v[i] / sc);
+}
+
+void orc_pack_w8(const float* w, int64_t rows, int64_t K, uint8_t* q, float* s) {
+    for (int64_t r = 0; r < rows; ++r) quant_row_fp8(w + r * K, K, q + r * K, s + r);
+}
+
+void orc_quant_rows_fp8(const float* x, int64_t n, int64_t K, uint8_t* q, float* a) {
+    for (int64_t r = 0; r < n; ++r) quant_row_fp8(x + r * K, K, q + r * K, a + r);
+}
+
+/* v = (acc * a) * s_w with acc the fp32 ascending sum of exact products. */
+static float dot_w8_row(const uint8_t* xq, float a, const uint8_t* q_row, float s_row, int64_t K) {
+    float acc = 0.0f;
+    for (int64_t i = 0; i < K; ++i) acc += orc_e4m3_to_f32(q_row[i]) * orc_e4m3_to_f32(xq[i]);
+    return (acc * a) * s_row;
+}
+
+void orc_expert_token_w8a8(const uint16_t* x, int32_t d, int32_t F, const uint8_t* q_gu,
+                           const float* s_gu, const uint8_t* q_dn, const float* s_dn, uint16_t* h,
+                           float* y) {
+    float* xf = (float*)malloc(sizeof(float) * (size_t)d);
+    float* hf = (float*)malloc(sizeof(float) * (size_t)F);
+    uint8_t* xq = (uint8_t*)malloc((size_t)d);
+    uint8_t* hq = (uint8_t*)malloc((size_t)F);
+    float a_x, a_h;
+    for (int32_t i = 0; i < d; ++i) xf[i] = orc_bf16_to_f32(x[i]);
+    quant_row_fp8(xf, d, xq, &a_x);
+    for (int32_t f = 0; f < F; ++f) {
+        float g = dot_w8_row(xq, a_x, q_gu + (int64_t)f * d, s_gu[f], d);
+        float u = dot_w8_row(xq, a_x, q_gu + (int64_t)(F + f) * d, s_gu[F + f], d);
+        double silu = (double)g / (1.0 + exp(-(double)g));
+        h[f] = orc_f64_to_bf16(silu * (double)u);
+        hf[f] = orc_bf16_to_f32(h[f]);
+    }
+    quant_row_fp8(hf, F, hq, &a_h);
+    for (int32_t c = 0; c < d; ++c) y[c] = dot_w8_row(hq, a_h, q_dn + (int64_t)c * F, s_dn[c], F);
+    free(xf);
+    free(hf);
+    free(xq);
+    free(hq);
+}
+
+void orc_layer_w8a8_tokens(const uint16_t* x, int32_t d, int32_t k, int32_t F, int32_t Fs,
+                           const int32_t* topk_idx, const float* topk_w, const uint8_t* q_gu,
+                           const float* s_gu, const uint8_t* q_dn, const float* s_dn,
+                           const uint8_t* qs_gu, const float* ss_gu, const uint8_t* qs_dn,
+                           const float* ss_dn, const int64_t* tokens, int64_t n_tokens,
+                           uint16_t* out, uint16_t* h_routed, uint16_t* h_shared) {
+    int64_t gu_bytes = (int64_t)2 * F * d, dn_bytes = (int64_t)d * F;
+    float* y = (float*)malloc(sizeof(float) * (size_t)d);
+    float* acc = (float*)malloc(sizeof(float) * (size_t)d);
+    uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(F > Fs ? F : Fs));
+    for (int64_t n = 0; n < n_tokens; ++n) {
+        int64_t t = tokens[n];
+        const uint16_t* xt = x + t * d;
+        for (int32_t c = 0; c < d; ++c) acc[c] = 0.0f;
+        for (int32_t j = 0; j < k; ++j) {
+            int64_t e = topk_idx[t * k + j];
+            float wj = topk_w[t * k + j];
+            orc_expert_token_w8a8(xt, d, F, q_gu + e * gu_bytes, s_gu + e * 2 * F,
+                                  q_dn + e * dn_bytes, s_dn + e * d, h, y);
+            if (h_routed) memcpy(h_routed + (n * k + j) * F, h, sizeof(uint16_t) * (size_t)F);
+            for (int32_t c = 0; c < d; ++c) {
+                float p = wj * y[c];
+                acc[c] = acc[c] + p;
+            }
+        }
+        orc_expert_token_w8a8(xt, d, Fs, qs_gu, ss_gu, qs_dn, ss_dn, h, y);
+        if (h_shared) memcpy(h_shared + n * Fs, h, sizeof(uint16_t) * (size_t)Fs);
+        for (int32_t c = 0; c < d; ++c) {
+            acc[c] = acc[c] + y[c];
+            out[n * d + c] = orc_f32_to_bf16(acc[c]);
+        }
+    }
+    free(y);
+    free(acc);
+    free(h);
+}
+
+void orc_f32_to_e4m3_array(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_e4m3(x[i]);
+}
+void orc_e4m3_to_f32_array(const uint8_t* b, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_to_f32(b[i]);
 }
 
 /* ------------------------------------------------------------------ */

@@ -79,6 +79,27 @@ void orc_layer_tokens(const uint16_t* x, int32_t d, int32_t E, int32_t k, int32_
                       const int64_t* tokens, int64_t n_tokens, uint16_t* out, uint16_t* h_routed,
                       uint16_t* h_shared);
 
+
+/* W8A8 (fp8 E4M3 weights and activations, reading R16): per-row scales
+   (absmax / 448, fp32), codes E4M3 rounded to nearest even and saturated to
+   +-448.  Weights q [rows][K] bytes, s fp32 [rows]; a layer's routed gate+up
+   codes are [E][2F][d] with scales [E][2F], down [E][d][F] with [E][d]. */
+float orc_e4m3_to_f32(uint8_t b);
+uint8_t orc_f32_to_e4m3(float x);
+void orc_pack_w8(const float* w, int64_t rows, int64_t K, uint8_t* q, float* s);
+void orc_quant_rows_fp8(const float* x, int64_t n, int64_t K, uint8_t* q, float* a);
+void orc_expert_token_w8a8(const uint16_t* x, int32_t d, int32_t F, const uint8_t* q_gu,
+                           const float* s_gu, const uint8_t* q_dn, const float* s_dn, uint16_t* h,
+                           float* y);
+void orc_layer_w8a8_tokens(const uint16_t* x, int32_t d, int32_t k, int32_t F, int32_t Fs,
+                           const int32_t* topk_idx, const float* topk_w, const uint8_t* q_gu,
+                           const float* s_gu, const uint8_t* q_dn, const float* s_dn,
+                           const uint8_t* qs_gu, const float* ss_gu, const uint8_t* qs_dn,
+                           const float* ss_dn, const int64_t* tokens, int64_t n_tokens,
+                           uint16_t* out, uint16_t* h_routed, uint16_t* h_shared);
+void orc_f32_to_e4m3_array(const float* x, int64_t n, uint8_t* out);
+void orc_e4m3_to_f32_array(const uint8_t* b, int64_t n, float* out);
+
 /* Element-wise array forms of the format conversions. */
 void orc_f32_to_f16_array(const float* x, int64_t n, uint16_t* out);
 void orc_f16_to_f32_array(const uint16_t* h, int64_t n, float* out);
