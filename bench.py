@@ -42,6 +42,9 @@ import workloads  # noqa: E402
 
 HEADLINE = "decode1"
 SECONDARY = "decode32,prefill2048,skew8192"
+# secondary configs also timed with the W8A8 experts (fp8 weights and activations)
+W8A8_CONFIGS = ("prefill2048", "skew8192")
+FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 # steps per timed window of each secondary config (about 0.1-0.5 s each)
 SECONDARY_STEPS = {"decode1": 4000, "decode32": 1000, "prefill2048": 300, "skew8192": 60,
                    "tiny": 4000}
@@ -123,8 +126,10 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
-def kernels_per_step(cfg, flags=0):
+def kernels_per_step(cfg, flags=0, fmt="w4"):
     """Kernels libmoe.so launches for one moe_layer_forward (memset nodes excluded)."""
+    if fmt == "w8":  # router (2), descriptors (4), x quantiser, GEMM, H quantiser, GEMM, combine
+        return 2 + 4 + 1 + 1 + 1 + 1 + 1
     gemv = (flags & 0x1) or (cfg.T <= 4 and not flags & 0x2)
     if gemv and cfg.T == 1 and flags & 0x8:
         return 1  # the cooperative single-launch step
@@ -136,7 +141,7 @@ def kernels_per_step(cfg, flags=0):
 
 
 class GpuBench:
-    def __init__(self, cfg, device, ncopy: int, nbatch: int, flags: int = 0):
+    def __init__(self, cfg, device, ncopy: int, nbatch: int, flags: int = 0, fmt: str = "w4"):
         import torch
 
         import moe_expert_layer_sigmoid_gb300 as moe
@@ -145,33 +150,41 @@ class GpuBench:
         self.torch, self.moe = torch, moe
         self.cfg = cfg
         self.device = device
-        self.layer = upload(cfg, device=device, extra_batches=nbatch - 1)
+        self.fmt = fmt
+        self.layer = upload(cfg, device=device, extra_batches=nbatch - 1, fmt=fmt)
         L = self.layer
         self.xs = [L.x] + list(L.x_batches)
         # weight copies: copy 0 is the uploaded one; every copy has its own router
         # weights too, as every layer of a model does, so none stays in L2
-        self.copies = [L.w4s()]
+        wrap = moe.w8 if fmt == "w8" else moe.w4
+        self.copies = [L.w8s() if fmt == "w8" else L.w4s()]
         self.routers = [(L.W_r, L.bias)]
         self._keep = []
         for _ in range(ncopy - 1):
             ts = [t.clone() for t in (L.gu_q, L.gu_s, L.dn_q, L.dn_s, L.sgu_q, L.sgu_s, L.sdn_q,
                                       L.sdn_s, L.W_r, L.bias)]
             self._keep.append(ts)
-            self.copies.append((moe.w4(ts[0], ts[1]), moe.w4(ts[2], ts[3]), moe.w4(ts[4], ts[5]),
-                                moe.w4(ts[6], ts[7])))
+            self.copies.append((wrap(ts[0], ts[1]), wrap(ts[2], ts[3]), wrap(ts[4], ts[5]),
+                                wrap(ts[6], ts[7])))
             self.routers.append((ts[8], ts[9]))
         self.dims = L.dims()
         self.dims.flags = flags
-        self.ws = moe.workspace(moe.moe_layer_workspace_bytes(self.dims), device)
+        self.ws_bytes = (moe.moe_layer_workspace_bytes_w8a8 if fmt == "w8" else
+                         moe.moe_layer_workspace_bytes)
+        self.ws = moe.workspace(self.ws_bytes(self.dims), device)
         self.out = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=device)
         self.stream = torch.cuda.Stream(device)
         self.nslots = max(len(self.copies), len(self.xs))
+        # the copies were made on the current stream; the steps run on self.stream, which
+        # does not wait for it
+        torch.cuda.synchronize(device)
 
     def step(self, i, stream=None):
         c = self.copies[i % len(self.copies)]
         wr, bias = self.routers[i % len(self.routers)]
         x = self.xs[i % len(self.xs)]
-        self.moe.moe_layer_forward(x, wr, bias, self.dims, *c, self.out, self.ws, stream=stream)
+        fwd = self.moe.moe_layer_forward_w8a8 if self.fmt == "w8" else self.moe.moe_layer_forward
+        fwd(x, wr, bias, self.dims, *c, self.out, self.ws, stream=stream)
 
     def capture(self):
         """One graph per slot, and one graph of all slots in a row (so that a
@@ -257,7 +270,7 @@ class GpuBench:
         moe, torch = self.moe, self.torch
         T, k, E = self.cfg.T, self.cfg.k, self.cfg.E
         dims = self.dims
-        ws = moe.workspace(moe.moe_workspace_bytes(dims), self.device)
+        ws = moe.workspace(self.ws_bytes(dims), self.device)
         i32 = dict(dtype=torch.int32, device=self.device)
         idx = torch.empty((T, k), **i32)
         w = torch.empty((T, k), dtype=torch.float32, device=self.device)
@@ -282,9 +295,13 @@ class GpuBench:
         def launch(i):
             dsc = descs[i % self.nslots]
             c = self.copies[i % len(self.copies)]
-            moe.moe_gateup_swiglu_w4a16(self.xs[i % len(self.xs)], self.dims, dsc["offsets"],
-                                        dsc["perm"], dsc["sched"], c[0], c[2], H, dsc["ws"],
-                                        stream=self.stream)
+            if self.fmt == "w8":
+                moe.moe_gateup_swiglu_w8a8(self.xs[i % len(self.xs)], self.dims, dsc["perm"],
+                                           c[0], c[2], H, dsc["ws"], stream=self.stream)
+            else:
+                moe.moe_gateup_swiglu_w4a16(self.xs[i % len(self.xs)], self.dims, dsc["offsets"],
+                                            dsc["perm"], dsc["sched"], c[0], c[2], H, dsc["ws"],
+                                            stream=self.stream)
 
         with torch.cuda.stream(self.stream):
             for i in range(self.nslots):
@@ -411,16 +428,17 @@ def gpu_roofline_prefill(cfg, gu_ms, pk, pk_kind):
 
 
 def measure_config(name, device, warmup, steps, ncopy, nbatch, pk, pk_kind, gpu_index, flags=0,
-                   ab_flags=None, min_time=MIN_TIMED_S):
+                   ab_flags=None, min_time=MIN_TIMED_S, fmt="w4"):
     """Layer step (median of windows, clocks sampled across them), the standalone gate+up
     launch, and the end-to-end host call, on one config.  With ab_flags, the layer step
     and the gate+up launch are timed again with those flags (same inputs)."""
     cfg = workloads.CONFIGS[name]
-    b = GpuBench(cfg, device, ncopy=ncopy, nbatch=nbatch, flags=flags)
+    b = GpuBench(cfg, device, ncopy=ncopy, nbatch=nbatch, flags=flags, fmt=fmt)
     b.capture()
     ms, per, clk = b.run(warmup, steps, ClockSampler(gpu_index), min_time)
     gu_ms, active = b.time_gateup(warmup, steps)
-    e2e_ms, h2d, d2h = b.e2e(warmup, steps)
+    # the host-buffer entry point is the W4A16 layer's
+    e2e_ms, h2d, d2h = b.e2e(warmup, steps) if fmt == "w4" else (None, 0, 0)
     layer_bytes = float(np.mean([(a + 1) * cfg.packed_expert_bytes() for a in active]))
     res = dict(cfg=cfg, ms=ms, windows=per, clocks=clk, gu_ms=gu_ms, active=active,
                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, layer_bytes=layer_bytes,
@@ -541,6 +559,32 @@ def roofline_of(res, ms, pk, pk_kind) -> dict:
     return roof
 
 
+def w8a8_entry(res, base, pk, pk_kind) -> dict:
+    """The W8A8 layer on the same workload, against the fp8 peak (the measured bf16
+    peak times the nominal fp8 / bf16 ratio) and against the W4A16 layer (base)."""
+    cfg = res["cfg"]
+    flops = 2.0 * 2 * cfg.d * (cfg.F * cfg.slots + cfg.Fs * cfg.T)
+    tf = flops / (res["gu_ms"] * 1e-3) / 1e12
+    peak = pk["bf16_tflops"] * FP8_OVER_BF16
+    layer_tf = cfg.flops() / (res["ms"] * 1e-3) / 1e12
+    return {
+        "experts": "W8A8: E4M3 weights (one scale per row) x E4M3 activations (one scale per "
+                   "row), tcgen05 kind::f8f6f4",
+        "value": round(cfg.T / (res["ms"] * 1e-3), 1), "unit": "tokens/s",
+        "us_per_layer": round(res["ms"] * 1e3, 2),
+        "layer_tflops": round(layer_tf, 2),
+        "timing": timing_dict(res),
+        "roofline": {"kernel": "gateup (grouped_w8a8_kernel)", "bound": "tensor",
+                     "achieved": round(tf, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 4), "traffic": None, "flops_per_launch": flops,
+                     "launch_us": round(res["gu_ms"] * 1e3, 2),
+                     "peak_source": f"{pk_kind} bf16_tflops x {FP8_OVER_BF16} (nominal fp8/bf16)"},
+        "speedup_vs_w4a16_layer": round(base["ms"] / res["ms"], 3),
+        "speedup_vs_w4a16_gateup": round(base["gu_ms"] / res["gu_ms"], 3),
+        "clocks": res["clocks"],
+    }
+
+
 def secondary_entry(res, pk, pk_kind) -> dict:
     cfg = res["cfg"]
     ms = res["ms"]
@@ -558,6 +602,8 @@ def secondary_entry(res, pk, pk_kind) -> dict:
         "clocks": res["clocks"],
         "e2e": e2e_dict(res),
     }
+    if "w8" in res:
+        ent["w8a8"] = w8a8_entry(res["w8"], res, pk, pk_kind)
     if "ab" in res:
         ab = res["ab"]
         ent["no_sched"] = {
@@ -618,6 +664,10 @@ def main():
     ap.add_argument("--ncopy", type=int, default=8)
     ap.add_argument("--nbatch", type=int, default=8)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--fmt", default="w4", choices=["w4", "w8"],
+                    help="expert weights of the headline config: int4 (W4A16) or fp8 (W8A8)")
+    ap.add_argument("--no-w8a8", action="store_true",
+                    help="skip the W8A8 timings of the prefill configs")
     ap.add_argument("--min-time", type=float, default=MIN_TIMED_S,
                     help="repeat timed windows for at least this many seconds (>= 5 windows)")
     ap.add_argument("--flags", type=int, default=0,
@@ -643,7 +693,7 @@ def main():
         dist.barrier()
     main_res = measure_config(args.config, device, args.warmup, args.steps, args.ncopy,
                               args.nbatch, pk, pk_kind, gpu_index, flags=args.flags,
-                              min_time=args.min_time)
+                              min_time=args.min_time, fmt=args.fmt)
     sec_names = [] if args.secondary in ("", "none", '""') else \
         [n for n in args.secondary.split(",") if n and n != args.config]
     sec_res = []
@@ -651,9 +701,12 @@ def main():
         steps = args.secondary_steps or SECONDARY_STEPS.get(name, 100)
         # the skewed config also runs without the grouped kernel's CTA scheduling
         ab = 0x4 if workloads.CONFIGS[name].bias == "zipf" else None
-        sec_res.append(measure_config(name, device, args.warmup, steps, args.ncopy, args.nbatch,
-                                      pk, pk_kind, gpu_index, ab_flags=ab,
-                                      min_time=args.min_time))
+        r = measure_config(name, device, args.warmup, steps, args.ncopy, args.nbatch, pk, pk_kind,
+                           gpu_index, ab_flags=ab, min_time=args.min_time)
+        if name in W8A8_CONFIGS and not args.no_w8a8:
+            r["w8"] = measure_config(name, device, args.warmup, steps, args.ncopy, args.nbatch, pk,
+                                     pk_kind, gpu_index, min_time=args.min_time, fmt="w8")
+        sec_res.append(r)
     ms = max_over_ranks(main_res["ms"], device)
     cfg = main_res["cfg"]
     value = world * cfg.T / (ms * 1e-3)
@@ -666,12 +719,15 @@ def main():
                          f"{sec:.1f} s of single-thread CPU work"}
 
     if rank == 0:
-        roof = roofline_of(main_res, ms, pk, pk_kind)
+        roof = (roofline_of(main_res, ms, pk, pk_kind) if args.fmt == "w4" else
+                w8a8_entry(main_res, main_res, pk, pk_kind)["roofline"])
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "us_per_layer": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int4 weights x bf16 activations, f32 accumulate",
+            "vs_baseline": None,
+            "dtype": ("int4 weights x bf16 activations, f32 accumulate" if args.fmt == "w4" else
+                      "e4m3 weights x e4m3 activations, f32 accumulate"),
             "data": "synthetic (seeded generator, random weights of the layer's shapes)",
             "config": config_dict(cfg, args.ncopy, args.nbatch),
             "parallelism": f"{world} replicas, no collective" if world > 1 else "single GPU",
@@ -679,9 +735,9 @@ def main():
             "roofline": roof,
             "active_experts_mean": float(np.mean(main_res["active"])),
             "clocks": main_res["clocks"],
-            "e2e": e2e_dict(main_res),
-            "gpu_launches": kernels_per_step(cfg, args.flags) * args.steps,
-            "kernels_per_step": kernels_per_step(cfg, args.flags),
+            "e2e": e2e_dict(main_res) if args.fmt == "w4" else None,
+            "gpu_launches": kernels_per_step(cfg, args.flags, args.fmt) * args.steps,
+            "kernels_per_step": kernels_per_step(cfg, args.flags, args.fmt),
             "cpu_baseline": cpu,
             "peaks": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback",
         }

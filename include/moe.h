@@ -113,6 +113,13 @@ typedef struct {
     const uint16_t* s;
 } moe_w4_t;
 
+/* fp8 weights of the W8A8 variant: q [rows][K] E4M3 codes, s fp32 [rows]
+   (one scale per row); q 16-byte and s 4-byte aligned. */
+typedef struct {
+    const uint8_t* q;
+    const float* s;
+} moe_w8_t;
+
 /* Human-readable name of a status code (static storage). */
 const char* moe_status_string(moe_status_t status);
 
@@ -387,6 +394,65 @@ moe_status_t moe_layer_forward_host(const uint16_t* x_host, const float* W_r, co
  * reported an error, MOE_OK otherwise.  For tests and debugging; it is the one
  * call that blocks the host. */
 moe_status_t moe_check_device_status(void* ws, size_t ws_bytes, void* stream);
+
+/* ============================================================================
+ * W8A8 variant: fp8 (E4M3) weights and activations on the tcgen05 fp8 tensor
+ * cores.  Source: the W8A8 grouped MoE of thewafflehaus/FFAI PR #72
+ * (Nemotron-H section: fp8 activations x fp8 weights, argmax unchanged), with
+ * the scale recipe of the same PR's per-channel FP8 commit (one weight scale
+ * per output channel, one activation scale per token row, folded in after the
+ * GEMM).  Numerics:
+ *  - E4M3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits, no infinities,
+ *    largest finite 448; conversions round to nearest even and saturate.
+ *  - a weight row w: s = absmax(w) / 448 (fp32), codes e4m3(w / s) (fp32
+ *    division); an all-zero row has s = 0 and codes 0.  Activation rows
+ *    (each token's x for gate+up, each H row for down) the same way, scale a.
+ *  - a projection is (acc * a) * s, acc = sum over K of code products in fp32
+ *    (each product exact); SwiGLU, H = bf16, routing, the shared expert and
+ *    the combine as in the W4A16 layer.
+ * The router and descriptors are the W4A16 layer's; the experts always run
+ * on the grouped tensor-core kernel (any T).
+ * ========================================================================= */
+
+/* moe_pack_w8 -- fp32 weights [rows][K] (device) to E4M3 codes q [rows][K]
+ * and fp32 row scales s [rows] (device).  K % 8 == 0; w 16-byte, q 8-byte and
+ * s 4-byte aligned (MOE_ERR_INVALID_ARG otherwise).  Routed gate+up weights
+ * are one call on [E*2F][d] (rows 0..F-1 of each expert the gate), down on
+ * [E*d][F]; the shared expert's [2F_s][d] and [d][F_s]. */
+moe_status_t moe_pack_w8(const float* w, int64_t rows, int64_t K, uint8_t* q, float* s,
+                         void* stream);
+
+/* moe_quant_rows_fp8 -- bf16 rows [rows][K] (device) to E4M3 codes
+ * [rows][K] and fp32 row scales [rows] (device), the activation quantisation
+ * the layer applies.  K % 8 == 0; x 16-byte, q 8-byte, a 4-byte aligned. */
+moe_status_t moe_quant_rows_fp8(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q,
+                                float* a, void* stream);
+
+/* Workspace of moe_layer_forward_w8a8 and of the two W8A8 step calls below
+   (0 for unsupported dims). */
+size_t moe_layer_workspace_bytes_w8a8(const moe_dims_t* dims);
+
+/* The W8A8 expert projections as separate calls, after moe_router_topk and
+ * moe_build_descriptors on a workspace of moe_layer_workspace_bytes_w8a8:
+ *   moe_gateup_swiglu_w8a8: quantises each gathered token row (perm order,
+ *     then the shared rows) and runs gate+up with SwiGLU into H, bf16
+ *     [T*k + T][max(F, F_s)], as moe_gateup_swiglu_w4a16;
+ *   moe_down_w8a8: quantises each H row and writes Y, fp32 [T*k + T][d], as
+ *     moe_down_w4a16.
+ * Then moe_combine_shared (or its residual form) gives the layer output. */
+moe_status_t moe_gateup_swiglu_w8a8(const uint16_t* x, const moe_dims_t* dims,
+                                    const int32_t* perm, moe_w8_t Wgu, moe_w8_t Wgu_s,
+                                    uint16_t* H, void* ws, size_t ws_bytes, void* stream);
+moe_status_t moe_down_w8a8(const uint16_t* H, const moe_dims_t* dims, moe_w8_t Wd, moe_w8_t Wd_s,
+                           float* Y, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_layer_forward_w8a8 -- the whole layer with W8A8 experts.  Arguments as
+ * moe_layer_forward, the weights in moe_pack_w8's format.  Needs d, F, F_s
+ * multiples of 128 (MOE_ERR_UNSUPPORTED otherwise). */
+moe_status_t moe_layer_forward_w8a8(const uint16_t* x, const float* W_r, const float* bias,
+                                    const moe_dims_t* dims, moe_w8_t Wgu, moe_w8_t Wd,
+                                    moe_w8_t Wgu_s, moe_w8_t Wd_s, uint16_t* out, void* ws,
+                                    size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -38,7 +38,9 @@ EXPORTS = (
     "moe_layer_workspace_bytes", "moe_layer_forward", "moe_layer_forward_host",
     "moe_check_device_status", "moe_router_topk_noalloc", "moe_pack_w4_bytes",
     "moe_combine_shared_residual", "moe_layer_forward_residual", "moe_import_q4_blocks",
-    "moe_down_combine_w4a16",
+    "moe_down_combine_w4a16", "moe_pack_w8", "moe_quant_rows_fp8",
+    "moe_layer_workspace_bytes_w8a8", "moe_layer_forward_w8a8", "moe_gateup_swiglu_w8a8",
+    "moe_down_w8a8",
 )
 
 
@@ -65,6 +67,11 @@ class W4(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p)]
 
 
+class W8(ctypes.Structure):
+    """moe_w8_t: E4M3 codes and fp32 row scales (device pointers)."""
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -88,6 +95,12 @@ def lib() -> ctypes.CDLL:
         "moe_gateup_swiglu_w4a16": ([p, D, p, p, p, W4, W4, p, p, sz, p], i32),
         "moe_down_w4a16": ([p, D, p, p, W4, W4, p, p, sz, p], i32),
         "moe_down_combine_w4a16": ([p, D, p, p, p, p, W4, W4, p, p, p, sz, p], i32),
+        "moe_pack_w8": ([p, i64, i64, p, p, p], i32),
+        "moe_quant_rows_fp8": ([p, i64, i64, p, p, p], i32),
+        "moe_layer_workspace_bytes_w8a8": ([D], sz),
+        "moe_layer_forward_w8a8": ([p, p, p, D, W8, W8, W8, W8, p, p, sz, p], i32),
+        "moe_gateup_swiglu_w8a8": ([p, D, p, W8, W8, p, p, sz, p], i32),
+        "moe_down_w8a8": ([p, D, W8, W8, p, p, sz, p], i32),
         "moe_pack_w4_bytes": ([i64, i64, i32, ctypes.POINTER(sz)], sz),
         "moe_import_q4_blocks": ([p, i64, i64, i32, p, p, p, p], i32),
         "moe_combine_shared": ([p, p, p, D, p, p], i32),
@@ -144,6 +157,10 @@ def w4(q: torch.Tensor, s: torch.Tensor) -> W4:
     return W4(_dev(q, torch.uint8, "q"), _dev(s, torch.int16, "s"))
 
 
+def w8(q: torch.Tensor, s: torch.Tensor) -> W8:
+    return W8(_dev(q, torch.uint8, "q"), _dev(s, torch.float32, "s"))
+
+
 # ------------------------------------------------------------------ entry points
 
 def moe_pack_w4(w: torch.Tensor, group: int, q: torch.Tensor | None = None,
@@ -158,6 +175,57 @@ def moe_pack_w4(w: torch.Tensor, group: int, q: torch.Tensor | None = None,
                              _dev(q, torch.uint8, "q"), _dev(s, torch.int16, "s"),
                              _stream(stream)), "moe_pack_w4")
     return q, s
+
+
+def moe_pack_w8(w: torch.Tensor, q: torch.Tensor | None = None, s: torch.Tensor | None = None,
+                stream=None):
+    """fp32 [rows][K] -> (E4M3 codes uint8 [rows][K], fp32 row scales [rows])."""
+    rows, K = w.shape
+    if q is None:
+        q = torch.empty((rows, K), dtype=torch.uint8, device=w.device)
+    if s is None:
+        s = torch.empty(rows, dtype=torch.float32, device=w.device)
+    _check(lib().moe_pack_w8(_dev(w, torch.float32, "w"), rows, K, _dev(q, torch.uint8, "q"),
+                             _dev(s, torch.float32, "s"), _stream(stream)), "moe_pack_w8")
+    return q, s
+
+
+def moe_quant_rows_fp8(x: torch.Tensor, q: torch.Tensor | None = None,
+                       a: torch.Tensor | None = None, stream=None):
+    """bf16 rows (int16 bits) [rows][K] -> (E4M3 codes uint8 [rows][K], fp32 scales [rows])."""
+    rows, K = x.shape
+    if q is None:
+        q = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+    if a is None:
+        a = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(lib().moe_quant_rows_fp8(_dev(x, torch.int16, "x"), rows, K, _dev(q, torch.uint8, "q"),
+                                    _dev(a, torch.float32, "a"), _stream(stream)),
+           "moe_quant_rows_fp8")
+    return q, a
+
+
+def moe_layer_workspace_bytes_w8a8(dims: Dims) -> int:
+    return lib().moe_layer_workspace_bytes_w8a8(ctypes.byref(dims))
+
+
+def moe_layer_forward_w8a8(x, W_r, bias, dims: Dims, Wgu: W8, Wd: W8, Wgu_s: W8, Wd_s: W8, out,
+                           ws, stream=None):
+    _check(lib().moe_layer_forward_w8a8(
+        _dev(x, torch.int16, "x"), _dev(W_r, torch.float32, "W_r"), _dev(bias, torch.float32, "bias"),
+        ctypes.byref(dims), Wgu, Wd, Wgu_s, Wd_s, _dev(out, torch.int16, "out"), _ptr(ws),
+        ws.numel(), _stream(stream)), "moe_layer_forward_w8a8")
+
+
+def moe_gateup_swiglu_w8a8(x, dims: Dims, perm, Wgu: W8, Wgu_s: W8, H, ws, stream=None):
+    _check(lib().moe_gateup_swiglu_w8a8(
+        _dev(x, torch.int16, "x"), ctypes.byref(dims), _dev(perm, torch.int32, "perm"), Wgu, Wgu_s,
+        _dev(H, torch.int16, "H"), _ptr(ws), ws.numel(), _stream(stream)), "moe_gateup_swiglu_w8a8")
+
+
+def moe_down_w8a8(H, dims: Dims, Wd: W8, Wd_s: W8, Y, ws, stream=None):
+    _check(lib().moe_down_w8a8(
+        _dev(H, torch.int16, "H"), ctypes.byref(dims), Wd, Wd_s, _dev(Y, torch.float32, "Y"),
+        _ptr(ws), ws.numel(), _stream(stream)), "moe_down_w8a8")
 
 
 def moe_import_q4_blocks(blocks: torch.Tensor, K: int, group: int, w_scratch=None,

@@ -60,6 +60,13 @@ WsLayout ws_layout(const moe_dims_t& d) {
     L.out_stage = off;
     off += align256(sizeof(uint16_t) * (size_t)(T * d.d));
     L.layer_bytes = off;
+    L.w8_xa = off;
+    off += align256(sizeof(float) * (size_t)rows);
+    L.w8_hq = off;
+    off += align256((size_t)(rows * Fmax));
+    L.w8_ha = off;
+    off += align256(sizeof(float) * (size_t)rows);
+    L.w8a8_bytes = off;
     return L;
 }
 
@@ -146,6 +153,12 @@ moe_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
 bool w4_ok(moe_w4_t w) {
     return w.q && w.s && reinterpret_cast<uintptr_t>(w.q) % 16 == 0 &&
            reinterpret_cast<uintptr_t>(w.s) % 2 == 0;
+}
+
+// q is read by the TMA unit (16-byte aligned base), s with 4-byte loads.
+bool w8_ok(moe_w8_t w) {
+    return w.q && w.s && reinterpret_cast<uintptr_t>(w.q) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(w.s) % 4 == 0;
 }
 
 template <typename T>
@@ -470,6 +483,103 @@ moe_status_t moe_layer_forward_residual(const uint16_t* x, const float* W_r, con
     if (dims && dims->T > 0 && (!act_ok(residual) || !act_ok(out))) return MOE_ERR_INVALID_ARG;
     return layer_forward(x, W_r, bias, dims, Wgu, Wd, Wgu_s, Wd_s, residual, out, ws, ws_bytes,
                          stream);
+}
+
+moe_status_t moe_pack_w8(const float* w, int64_t rows, int64_t K, uint8_t* q, float* s,
+                         void* stream) {
+    if (rows < 0 || K <= 0 || K % 8) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!act_ok(w) || !q || !s || reinterpret_cast<uintptr_t>(q) % 8 ||
+        reinterpret_cast<uintptr_t>(s) % 4)
+        return MOE_ERR_INVALID_ARG;
+    return map_err(launch_quant_rows_fp8(w, false, rows, K, q, s, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quant_rows_fp8(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q, float* a,
+                                void* stream) {
+    if (rows < 0 || K <= 0 || K % 8) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!act_ok(x) || !q || !a || reinterpret_cast<uintptr_t>(q) % 8 ||
+        reinterpret_cast<uintptr_t>(a) % 4)
+        return MOE_ERR_INVALID_ARG;
+    return map_err(launch_quant_rows_fp8(x, true, rows, K, q, a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_layer_workspace_bytes_w8a8(const moe_dims_t* dims) {
+    if (check_dims(dims) != MOE_OK || !w8a8_supported(*dims)) return 0;
+    return ws_layout(*dims).w8a8_bytes;
+}
+
+moe_status_t moe_gateup_swiglu_w8a8(const uint16_t* x, const moe_dims_t* dims,
+                                    const int32_t* perm, moe_w8_t Wgu, moe_w8_t Wgu_s,
+                                    uint16_t* H, void* ws, size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    if (!w8a8_supported(*dims)) return MOE_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.w8a8_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!act_ok(x) || !perm || !act_ok(H) || !w8_ok(Wgu) || !w8_ok(Wgu_s))
+        return MOE_ERR_INVALID_ARG;
+    return map_err(launch_gateup_w8a8(x, *dims, perm, Wgu, Wgu_s, H, ws_at<WsHeader>(ws, L.header),
+                                      ws_at<int4>(ws, L.tiles), L.max_tiles,
+                                      ws_at<uint8_t>(ws, L.xs), ws_at<float>(ws, L.w8_xa),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_down_w8a8(const uint16_t* H, const moe_dims_t* dims, moe_w8_t Wd, moe_w8_t Wd_s,
+                           float* Y, void* ws, size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    if (!w8a8_supported(*dims)) return MOE_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.w8a8_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!act_ok(H) || !act_ok(Y) || !w8_ok(Wd) || !w8_ok(Wd_s)) return MOE_ERR_INVALID_ARG;
+    return map_err(launch_down_w8a8(H, *dims, Wd, Wd_s, Y, ws_at<WsHeader>(ws, L.header),
+                                    ws_at<int4>(ws, L.tiles) + L.max_tiles, L.max_tiles,
+                                    ws_at<uint8_t>(ws, L.w8_hq), ws_at<float>(ws, L.w8_ha),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_forward_w8a8(const uint16_t* x, const float* W_r, const float* bias,
+                                    const moe_dims_t* dims, moe_w8_t Wgu, moe_w8_t Wd,
+                                    moe_w8_t Wgu_s, moe_w8_t Wd_s, uint16_t* out, void* ws,
+                                    size_t ws_bytes, void* stream) {
+    moe_status_t st = check_dims(dims);
+    if (st != MOE_OK) return st;
+    if (!w8a8_supported(*dims)) return MOE_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(*dims);
+    if ((st = check_ws(ws, ws_bytes, L.w8a8_bytes)) != MOE_OK) return st;
+    if (dims->T == 0) return MOE_OK;
+    if (!act_ok(x) || !act_ok(W_r) || !bias || !act_ok(out) || !w8_ok(Wgu) || !w8_ok(Wd) ||
+        !w8_ok(Wgu_s) || !w8_ok(Wd_s))
+        return MOE_ERR_INVALID_ARG;
+    const moe_dims_t& d = *dims;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* topk_idx = ws_at<int32_t>(ws, L.topk_idx);
+    float* topk_w = ws_at<float>(ws, L.topk_w);
+    int32_t* pos = ws_at<int32_t>(ws, L.pos);
+    int32_t* perm = ws_at<int32_t>(ws, L.perm);
+    uint16_t* H = ws_at<uint16_t>(ws, L.H);
+    float* Y = ws_at<float>(ws, L.Y);
+    WsHeader* hdr = ws_at<WsHeader>(ws, L.header);
+    const int4* tiles = ws_at<int4>(ws, L.tiles);
+    cudaError_t e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
+                                  ws_at<float>(ws, L.logits), L.router_ksplit,
+                                  L.router_ksplit_large, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_descriptors(topk_idx, d, ws_at<int32_t>(ws, L.counts), ws_at<int32_t>(ws, L.offsets),
+                           perm, pos, ws_at<int32_t>(ws, L.sched), hdr, ws_at<int4>(ws, L.tiles),
+                           L.max_tiles, ws_at<int32_t>(ws, L.hist), s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_gateup_w8a8(x, d, perm, Wgu, Wgu_s, H, hdr, tiles, L.max_tiles,
+                           ws_at<uint8_t>(ws, L.xs), ws_at<float>(ws, L.w8_xa), s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_down_w8a8(H, d, Wd, Wd_s, Y, hdr, tiles + L.max_tiles, L.max_tiles,
+                         ws_at<uint8_t>(ws, L.w8_hq), ws_at<float>(ws, L.w8_ha), s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return map_err(launch_combine(Y, topk_w, pos, d, nullptr, out, s));
 }
 
 moe_status_t moe_layer_forward_host(const uint16_t* x_host, const float* W_r, const float* bias,

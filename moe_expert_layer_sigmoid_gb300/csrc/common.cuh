@@ -50,6 +50,10 @@ struct WsLayout {
     // whole-layer workspace (moe_layer_workspace_bytes) adds the intermediates
     size_t topk_idx, topk_w, counts, offsets, perm, pos, sched, H, Y, x_stage, out_stage;
     size_t layer_bytes;
+    // W8A8 layer (moe_layer_workspace_bytes_w8a8) adds the fp8 operands; the
+    // gate+up codes [T*k + T][d] reuse the xs region
+    size_t w8_xa, w8_hq, w8_ha;  // x row scales, H codes [T*k + T][max(F, F_s)], H row scales
+    size_t w8a8_bytes;
     int router_ksplit;    // K split of the small-T router
     int router_ksplit_large;  // K split of the large-T router
     int64_t max_tiles;    // capacity of each tile list
@@ -169,6 +173,19 @@ cudaError_t launch_gateup_grouped(const uint16_t* x, const moe_dims_t& d, const 
 cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t Wd,
                                 moe_w4_t Wd_s, float* Y, WsHeader* hdr, const int4* tiles,
                                 cudaStream_t st);
+
+// W8A8 grouped path (grouped_fp8.cu).  The gate+up launch quantises the
+// gathered token rows into xq / a, the down launch the H rows into hq / a.
+bool w8a8_supported(const moe_dims_t& d);
+cudaError_t launch_quant_rows_fp8(const void* src, bool bf16, int64_t rows, int64_t K, uint8_t* q,
+                                  float* s, cudaStream_t st);
+cudaError_t launch_gateup_w8a8(const uint16_t* x, const moe_dims_t& d, const int32_t* perm,
+                               moe_w8_t Wgu, moe_w8_t Wgu_s, uint16_t* H, WsHeader* hdr,
+                               const int4* tiles, int64_t max_tiles, uint8_t* xq, float* a,
+                               cudaStream_t st);
+cudaError_t launch_down_w8a8(const uint16_t* H, const moe_dims_t& d, moe_w8_t Wd, moe_w8_t Wd_s,
+                             float* Y, WsHeader* hdr, const int4* tiles, int64_t max_tiles,
+                             uint8_t* hq, float* a, cudaStream_t st);
 
 // `residual` (nullable, bf16 [T][d]) is added to the routed + shared sum
 // before the bf16 rounding; `out` may alias it.

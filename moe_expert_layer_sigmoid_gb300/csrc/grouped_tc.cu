@@ -57,6 +57,7 @@
 #include <mutex>
 
 #include "tma.cuh"
+#include "umma.cuh"
 
 namespace moe {
 namespace {
@@ -122,50 +123,6 @@ struct GroupedParams {
     int T, d, k, F, Fs, group;
 };
 
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// UMMA shared-memory descriptor: K-major operand, 128B swizzle, 8-row groups
-// 1024 B apart (SBO), descriptor version 1 (sm_100 family).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);  // start address
-    d |= (uint64_t)1 << 16;                   // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset
-    d |= (uint64_t)1 << 46;                   // version
-    d |= (uint64_t)2 << 61;                   // layout: 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4)                        // D format: f32
-           | (1u << 7)                      // A format: bf16
-           | (1u << 10)                     // B format: bf16
-           | ((uint32_t)(N >> 3) << 17)     // N / 8
-           | ((uint32_t)(M >> 4) << 24);    // M / 16
-}
-
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
 // ---------------------------------------------------------------- int4 -> bf16
 // One 32-bit word holds elements 0..7 (element 2j in the low nibble of byte
 // j).  Produces four bf16x2 registers {e_2j, e_2j+1} holding the exact
@@ -196,36 +153,6 @@ __device__ __forceinline__ void nib8_to_bf16x2_paired(uint32_t w, uint32_t* out)
         asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(t), "r"(0x3F803F80u), "r"(0xC308C308u));
         out[j] = q;
     }
-}
-
-// ---------------------------------------------------------------- TMEM copies
-__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t* v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {"
-        "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-        "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
-
-
-__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* v) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
-        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-          "=r"(v[31])
-        : "r"(taddr)
-        : "memory");
 }
 
 // ---------------------------------------------------------------- tiles

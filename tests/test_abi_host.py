@@ -214,3 +214,24 @@ def test_down_combine_validation(L):
     d0 = _dims(T=0)
     assert call(H=None, topk_w=None, pos=None, out=None, dims=d0,
                 nbytes=moe.moe_layer_workspace_bytes(d0)) == moe.MOE_OK
+
+
+def test_w8a8_entries_validate_before_launch(L):
+    ok, INV = 1 << 21, moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pack_w8(None, 0, 64, None, None, None) == moe.MOE_OK
+    assert L.moe_pack_w8(ok, 4, 60, ok, ok, None) == INV          # K % 8
+    assert L.moe_pack_w8(ok + 8, 4, 64, ok, ok, None) == INV      # w alignment
+    assert L.moe_pack_w8(ok, 4, 64, ok + 4, ok, None) == INV      # q alignment
+    assert L.moe_quant_rows_fp8(ok, 4, 64, ok, ok + 2, None) == INV
+    d = _dims()
+    need = moe.moe_layer_workspace_bytes_w8a8(d)
+    assert need > moe.moe_layer_workspace_bytes(d)
+    assert moe.moe_layer_workspace_bytes_w8a8(_dims(group=48)) == 0
+    w8 = moe.W8(ok, ok)
+    ws = 1 << 22
+    assert L.moe_layer_forward_w8a8(ok, ok, ok, ctypes.byref(d), w8, w8, w8, w8, ok, ws, need - 1,
+                                    None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_layer_forward_w8a8(ok, ok, ok, ctypes.byref(d), moe.W8(ok, ok + 2), w8, w8, w8,
+                                    ok, ws, need, None) == INV
+    assert L.moe_layer_forward_w8a8(ok + 8, ok, ok, ctypes.byref(d), w8, w8, w8, w8, ok, ws, need,
+                                    None) == INV
