@@ -130,7 +130,7 @@ def kernels_per_step(cfg, flags=0, fmt="w4"):
     """Kernels libmoe.so launches for one moe_layer_forward (memset nodes excluded)."""
     if fmt == "w8":  # router (2), descriptors (4), x quantiser, GEMM, H quantiser, GEMM, combine
         return 2 + 4 + 1 + 1 + 1 + 1 + 1
-    gemv = (flags & 0x1) or (cfg.T <= 4 and not flags & 0x2)
+    gemv = (flags & 0x1) or (cfg.T <= 3 and not flags & 0x2)
     if gemv and cfg.T == 1 and flags & 0x8:
         return 1  # the cooperative single-launch step
     if gemv and cfg.T <= 64:
@@ -617,6 +617,52 @@ def secondary_entry(res, pk, pk_kind) -> dict:
     return ent
 
 
+SWEEP_T = (1, 2, 3, 4, 6, 8, 16, 32, 64, 128, 256)
+
+
+def run_sweep(args, device, gpu_index):
+    """Layer time per step against T on each forced expert path (and the tensor-core
+    single-token step at T = 1), on one uploaded layer of the decode shapes: the
+    weights of decode1's seed, x the first T rows of each 256-token batch."""
+    import dataclasses
+
+    import torch
+    base = workloads.CONFIGS[args.config]
+    tmax = max(SWEEP_T)
+    cfg = dataclasses.replace(base, name=f"{base.name}_sweep", T=tmax)
+    b = GpuBench(cfg, device, ncopy=args.ncopy, nbatch=args.nbatch)
+    moe = b.moe
+    full_x, full_out = list(b.xs), b.out
+    paths = [("gemv", 0x1), ("grouped", 0x2)]
+    rows = []
+    for T in SWEEP_T:
+        for name, flags in paths + ([("mma_step", 0x9)] if T == 1 else []):
+            dims = b.layer.dims(flags, T=T)
+            if moe.moe_layer_workspace_bytes(dims) > b.ws.numel():
+                continue
+            b.dims = dims
+            b.xs = [x[:T] for x in full_x]
+            b.out = full_out[:T]
+            b.capture()
+            # about 0.2 s per window
+            t0 = time.perf_counter()
+            with torch.cuda.stream(b.stream):
+                b.replay_steps(b.nslots)
+            torch.cuda.synchronize(device)
+            est = max((time.perf_counter() - t0) / b.nslots, 1e-6)
+            steps = int(min(20000, max(b.nslots, 0.2 / est)))
+            ms, per, _ = b.run(args.warmup, steps, None, 0.0)
+            rows.append({"T": T, "path": name, "us_per_layer": round(ms * 1e3, 2),
+                         "tokens_per_s": round(T / (ms * 1e-3), 1), "windows": len(per),
+                         "steps_per_window": steps})
+            print(f"T={T:4d} {name:9s} {ms * 1e3:10.2f} us", file=sys.stderr, flush=True)
+    b.free()
+    print(json.dumps({"sweep": rows, "workload": f"{base.name} shapes, T = 1..{tmax}",
+                      "l2": f"{args.ncopy} weight copies x {args.nbatch} batches rotated"}),
+          flush=True)
+    return 0
+
+
 REF_BUDGET_S = 120.0  # cap on the reference arm's timed oracle work
 
 
@@ -666,6 +712,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--fmt", default="w4", choices=["w4", "w8"],
                     help="expert weights of the headline config: int4 (W4A16) or fp8 (W8A8)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the layer against T on each forced expert path (one JSON line)")
     ap.add_argument("--no-w8a8", action="store_true",
                     help="skip the W8A8 timings of the prefill configs")
     ap.add_argument("--min-time", type=float, default=MIN_TIMED_S,
@@ -689,6 +737,8 @@ def main():
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if "CUDA_VISIBLE_DEVICES" in os.environ else local
 
+    if args.sweep:
+        return run_sweep(args, device, gpu_index)
     if world > 1:
         dist.barrier()
     main_res = measure_config(args.config, device, args.warmup, args.steps, args.ncopy,

@@ -64,12 +64,13 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Router tiling: T <= kRouterSmallT uses the split-K GEMV form.
 constexpr int kRouterSmallT = 64;
 
-// GEMV (decode) expert path by default for T <= kGemvMaxT (the CUDA-core GEMV
-// redoes its dequantisation per 4-token pass and is FMA-bound beyond a few
-// tokens: at T = 32 the grouped tensor-core kernel measured 6x faster); the
-// flags can force it for any T <= kMaxDecodeT.  One pass of its loads covers
-// rows of up to kGemvMaxD (gate+up) / kGemvMaxF (down) elements.
-constexpr int kGemvMaxT = 4;
+// GEMV (decode) expert path by default for T <= kGemvMaxT, from a sweep of the
+// layer time over T on both forced paths at the decode shapes (GB300): the
+// CUDA-core GEMV took 35.8 / 79 / 110 / 145 us at T = 1 / 2 / 3 / 4 (its
+// multi-token form is FMA-bound, ~36 us per token), the grouped tensor-core
+// kernel 97 / 104 / 112 / 122 us; the flags can force either.  One pass of the
+// GEMV's loads covers rows of up to kGemvMaxD (gate+up) / kGemvMaxF (down).
+constexpr int kGemvMaxT = 3;
 constexpr int kGemvMaxD = 4096;
 constexpr int kGemvMaxF = 2048;
 

@@ -65,6 +65,8 @@ enum F8Mode : int { kF8GateUp = 0, kF8Down = 1 };
 
 struct F8Params {
     CUtensorMap tm_b;        // activation codes [rows][K] bytes, box {128, 128}
+    CUtensorMap tm_b32;      // box {128, 32}: tiles of at most 32 tokens
+    CUtensorMap tm_b64;      // box {128, 64}: tiles of 33-64 tokens
     CUtensorMap tm_a;        // routed weight codes (gate+up 5D, down 2D)
     CUtensorMap tm_a_sh;     // shared-expert weight codes, same boxes
     const float* s_routed;   // weight row scales [E * rows_per_expert]
@@ -79,6 +81,13 @@ struct F8Params {
     int mode;
     int T, d, k, E, F, Fs;
 };
+
+// Activation rows a stage loads for a tile: the smallest box of 32, 64 or 128
+// rows holding its npad tokens (the MMA reads npad rows).
+__device__ __forceinline__ int f8_box_rows(int n) {
+    const int npad = (n + 15) & ~15;
+    return npad <= 32 ? 32 : npad <= 64 ? 64 : 128;
+}
 
 // A tile the descriptors could have written: a group id in [-1, E), 1..128
 // tokens inside the activation rows, a weight band inside the group's rows.
@@ -119,6 +128,8 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
         prefetch_tmap(&p.tm_a);
         prefetch_tmap(&p.tm_a_sh);
         prefetch_tmap(&p.tm_b);
+        prefetch_tmap(&p.tm_b32);
+        prefetch_tmap(&p.tm_b64);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -150,6 +161,8 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                 }
                 const int grp = t.x, row0 = t.y, band = t.w;
                 const CUtensorMap* tma = grp >= 0 ? &p.tm_a : &p.tm_a_sh;
+                const int brows = f8_box_rows(t.z);
+                const CUtensorMap* tmb = brows == 32 ? &p.tm_b32 : brows == 64 ? &p.tm_b64 : &p.tm_b;
                 const int nks = tile_K(grp) / kF8K;
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     const int s = it % kF8Stages;
@@ -158,7 +171,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(kF8BarFull + s), (uint32_t)(kF8ABytes + kF8BBytes));
+                    mbar_expect_tx(bar(kF8BarFull + s), (uint32_t)(kF8ABytes + brows * kF8K));
                     const uint32_t adst = sbase + kF8OffA + s * kF8ABytes;
                     if (gateup)  // rows m = 32 * blk + 16 * gu + i
                         tma_load_5d(adst, tma, ks * kF8K, 0, 0, 4 * band, grp >= 0 ? grp : 0,
@@ -166,7 +179,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                     else
                         tma_load_2d(adst, tma, ks * kF8K, (grp >= 0 ? grp * p.d : 0) + 128 * band,
                                     bar(kF8BarFull + s));
-                    tma_load_2d(sbase + kF8OffB + s * kF8BBytes, &p.tm_b, ks * kF8K, row0,
+                    tma_load_2d(sbase + kF8OffB + s * kF8BBytes, tmb, ks * kF8K, row0,
                                 bar(kF8BarFull + s));
                 }
             }
@@ -385,10 +398,10 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const Src* __restrict__
 
 // ---------------------------------------------------------------- host side
 bool make_codes_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
-                    uint64_t row_bytes) {
+                    uint64_t row_bytes, uint32_t box_rows = 128) {
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)kF8K, 128};
+    const cuuint32_t box[2] = {(cuuint32_t)kF8K, box_rows};
     return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box,
                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -445,6 +458,8 @@ cudaError_t launch_gateup_w8a8(const uint16_t* x, const moe_dims_t& d, const int
     F8Params prm;
     memset(&prm, 0, sizeof(prm));
     if (!make_codes_map(&prm.tm_b, xq, d.d, rows, d.d) ||
+        !make_codes_map(&prm.tm_b32, xq, d.d, rows, d.d, 32) ||
+        !make_codes_map(&prm.tm_b64, xq, d.d, rows, d.d, 64) ||
         !make_gateup_codes_map(&prm.tm_a, Wgu.q, d.d, d.F, d.E) ||
         !make_gateup_codes_map(&prm.tm_a_sh, Wgu_s.q, d.d, d.F_s, 1))
         return cudaErrorInvalidValue;
@@ -474,6 +489,8 @@ cudaError_t launch_down_w8a8(const uint16_t* H, const moe_dims_t& d, moe_w8_t Wd
     F8Params prm;
     memset(&prm, 0, sizeof(prm));
     if (!make_codes_map(&prm.tm_b, hq, Fmax, rows, Fmax) ||
+        !make_codes_map(&prm.tm_b32, hq, Fmax, rows, Fmax, 32) ||
+        !make_codes_map(&prm.tm_b64, hq, Fmax, rows, Fmax, 64) ||
         !make_codes_map(&prm.tm_a, Wd.q, d.F, (uint64_t)d.E * d.d, d.F) ||
         !make_codes_map(&prm.tm_a_sh, Wd_s.q, d.F_s, (uint64_t)d.d, d.F_s))
         return cudaErrorInvalidValue;

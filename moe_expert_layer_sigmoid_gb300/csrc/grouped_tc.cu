@@ -111,6 +111,8 @@ enum Mode : int { kGateUp = 0, kDown = 1 };
 
 struct GroupedParams {
     CUtensorMap tm_b;        // activation rows (gathered x or H), bf16, box {64, 128}, 128B swizzle
+    CUtensorMap tm_b32;      // the same rows, box {64, 32}: tiles of at most 32 tokens
+    CUtensorMap tm_b64;      // box {64, 64}: tiles of 33-64 tokens
     CUtensorMap tm_a;        // routed int4 weights, uint8 rows; gate+up box {64, 16}, down {64, 128}
     CUtensorMap tm_a_sh;     // shared-expert int4 weights, same boxes
     const __half* s_routed;  // [E * rows_per_expert][K / group]
@@ -179,6 +181,11 @@ __device__ __forceinline__ TileInfo decode_tile(const GroupedParams& p, int4 t) 
     return ti;
 }
 
+// Activation rows one stage loads for a tile: the smallest box of 32, 64 or 128
+// rows that holds its npad tokens (the MMA reads npad rows; smaller boxes keep
+// small-token tiles from moving 128 rows per stage).
+__device__ __forceinline__ int b_box_rows(int npad) { return npad <= 32 ? 32 : npad <= 64 ? 64 : 128; }
+
 __device__ __forceinline__ int4 load_tile(const GroupedParams& p, int tile, int n_tiles) {
     return tile < n_tiles ? __ldg(p.tiles + tile) : make_int4(0, 0, 1, 0);
 }
@@ -232,6 +239,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_a)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_a_sh)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_b)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_b32)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_b64)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -287,7 +296,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                         const int s = it % kStages;
                         const uint32_t ph = (it / kStages) & 1;
                         if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1, abort_flag, p.hdr)) { ok = false; break; }
-                        mbar_expect_tx(bar(kBarFull + s), (uint32_t)(kAStageBytes + kBStageBytes));
+                        const int brows = b_box_rows(ti.npad);
+                        mbar_expect_tx(bar(kBarFull + s), (uint32_t)(kAStageBytes + brows * 256));
                         // one box each: the weight tile and both 64-wide K blocks of the activations
                         const uint32_t adst = sbase + kOffA + s * kAStageBytes;
                         if (p.mode == kGateUp)  // rows m = 32*blk + 16*gu + i (gate/up interleaved)
@@ -295,7 +305,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                                         bar(kBarFull + s));
                         else
                             tma_load_2d(adst, tma, ks * 64, weight_row(p, ti, 0, 0), bar(kBarFull + s));
-                        tma_load_3d(sbase + kOffB + s * kBStageBytes, &p.tm_b, 0, ti.row0, 2 * ks,
+                        tma_load_3d(sbase + kOffB + s * kBStageBytes,
+                                    brows == 32 ? &p.tm_b32 : brows == 64 ? &p.tm_b64 : &p.tm_b, 0, ti.row0, 2 * ks,
                                     bar(kBarFull + s));
                     }
                     cur = nxt;
@@ -322,6 +333,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     const int4 nxt = load_tile(p, tile + grid, n_tiles);
                     const TileInfo ti = decode_tile<G>(p, cur);
                     const uint32_t idesc = idesc_bf16(128, ti.npad);
+                    // 16-byte units between the stage's two 64-wide K blocks of B
+                    const int kb_units = b_box_rows(ti.npad) * 8;
                     const int nks = ti.K / kKStage;
                     for (int ks = 0; ks < nks && ok; ++ks, ++it) {
                         const int s = it % kStages;
@@ -337,8 +350,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                         // B tile before the MMAs
                         if (!mbar_wait(bar(kBarAReady + ta), tph, abort_flag, p.hdr)) { ok = false; break; }
                         tc_fence_after();
-                        // descriptor of the stage's B tile; K steps add (kg/4)*16 KB + (kg%4)*32 B,
-                        // i.e. (kg/4)*1024 + (kg%4)*2 in the 16-byte address field
+                        // descriptor of the stage's B tile; K steps add (kg/4) K blocks (box rows x
+                        // 128 B each) + (kg%4)*32 B, in units of 16 bytes
                         const uint64_t bdesc0 = smem_desc_sw128(sbase + kOffB + s * kBStageBytes);
                         const uint32_t a0 = tmem + (uint32_t)(ta * 64);
     #pragma unroll
@@ -355,7 +368,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                             for (int kk = 0; kk < G / 16; ++kk) {
                                 const int kg = gg * (G / 16) + kk;  // 16-wide K step within the stage
                                 mma_ts(dcol, a0 + (uint32_t)(kg * 8),
-                                       bdesc0 + (uint64_t)((kg >> 2) * 1024 + (kg & 3) * 2), idesc,
+                                       bdesc0 + (uint64_t)((kg >> 2) * kb_units + (kg & 3) * 2), idesc,
                                        kk > 0 ? 1u : 0u);
                             }
                             mma_commit(bar(kBarDFull + b));
@@ -589,14 +602,21 @@ bool make_map_nd(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int r
 
 namespace {
 
-// Activation rows [rows][cols] bf16 read as {64 elements, 128 rows, 2 K blocks}:
-// one box fills both 64-wide K blocks of a stage.
-bool make_act_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+// Activation rows [rows][cols] bf16 read as {64 elements, box_rows rows, 2 K
+// blocks}: one box fills both 64-wide K blocks of a stage.
+bool make_act_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                  uint32_t box_rows) {
     const cuuint64_t dims[3] = {64, rows, cols / 64};
     const cuuint64_t strides[2] = {cols * 2, 128};
-    const cuuint32_t box[3] = {64, kTokTile, 2};
+    const cuuint32_t box[3] = {64, box_rows, 2};
     return make_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 3, dims, strides, box,
                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_act_maps(GroupedParams& prm, const void* base, uint64_t cols, uint64_t rows) {
+    return make_act_map(&prm.tm_b, base, cols, rows, kTokTile) &&
+           make_act_map(&prm.tm_b32, base, cols, rows, 32) &&
+           make_act_map(&prm.tm_b64, base, cols, rows, 64);
 }
 
 // Gate+up int4 weights of `experts` experts ([experts][2Fg][d/2] bytes) read as
@@ -674,7 +694,7 @@ cudaError_t launch_gateup_grouped(const uint16_t* x, const moe_dims_t& d, const 
     GroupedParams prm;
     memset(&prm, 0, sizeof(prm));
     const int Fmax = std::max(d.F, d.F_s);
-    if (!make_act_map(&prm.tm_b, xs, d.d, rows) ||
+    if (!make_act_maps(prm, xs, d.d, rows) ||
         !make_gateup_map(&prm.tm_a, Wgu.q, d.d, d.F, d.E) ||
         !make_gateup_map(&prm.tm_a_sh, Wgu_s.q, d.d, d.F_s, 1))
         return cudaErrorInvalidValue;
@@ -696,7 +716,7 @@ cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t
     memset(&prm, 0, sizeof(prm));
     const int Fmax = std::max(d.F, d.F_s);
     const uint64_t rows = (uint64_t)d.T * d.k + d.T;
-    if (!make_act_map(&prm.tm_b, H, Fmax, rows) ||
+    if (!make_act_maps(prm, H, Fmax, rows) ||
         !make_map(&prm.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wd.q, d.F / 2, (uint64_t)d.E * d.d,
                   d.F / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&prm.tm_a_sh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wd_s.q, d.F_s / 2, (uint64_t)d.d,

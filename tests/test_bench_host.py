@@ -79,7 +79,7 @@ def test_reference_config_is_the_gpu_arms_config():
     assert "seed 1" in d["config"]["workload"]
 
 
-@pytest.mark.parametrize("name,flags,n", [("decode1", 0, 3), ("tiny", 0, 3), ("decode32", 0, 10),
+@pytest.mark.parametrize("name,flags,n", [("decode1", 0, 3), ("tiny", 0, 10), ("decode32", 0, 10),
                                           ("prefill2048", 0, 10), ("decode32", 1, 3),
                                           ("decode1", 2, 10), ("decode1", 8, 1)])
 def test_kernels_per_step(name, flags, n):
