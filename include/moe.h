@@ -395,6 +395,24 @@ moe_status_t moe_layer_forward_host(const uint16_t* x_host, const float* W_r, co
  * call that blocks the host. */
 moe_status_t moe_check_device_status(void* ws, size_t ws_bytes, void* stream);
 
+/* moe_debug_set_waits -- test hook for the bounded waits.  Every mbarrier wait
+ * in the grouped kernels gives up after a limit (2 s by default), records a
+ * wait timeout in the workspace header (moe_check_device_status then returns
+ * MOE_ERR_DEVICE_CHECK) and ends its kernel in order: the other roles leave at
+ * their next wait, the copy and MMA issuers wait (bounded) for their own work
+ * in flight, TMEM is freed.  This
+ * call stores, in the workspace header (stream-ordered, graph-capturable):
+ *   wait_ns         the limit of every such wait using this workspace (0: the
+ *                   default);
+ *   withhold_stage  s > 0: in every later gate+up launch on the grouped path
+ *                   (W4A16 and W8A8), CTA 0 skips the copies of its s-th
+ *                   pipeline stage, so that stage's consumers wait until the
+ *                   limit; 0: off.
+ * No memory access changes.  A call with (0, 0) restores normal operation; the
+ * workspace stays usable (moe_check_device_status clears the flag). */
+moe_status_t moe_debug_set_waits(void* ws, size_t ws_bytes, uint64_t wait_ns,
+                                 int32_t withhold_stage, void* stream);
+
 /* ============================================================================
  * W8A8 variant: fp8 (E4M3) weights and activations on the tcgen05 fp8 tensor
  * cores.  Source: the W8A8 grouped MoE of thewafflehaus/FFAI PR #72

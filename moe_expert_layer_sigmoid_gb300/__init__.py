@@ -40,7 +40,7 @@ EXPORTS = (
     "moe_combine_shared_residual", "moe_layer_forward_residual", "moe_import_q4_blocks",
     "moe_down_combine_w4a16", "moe_pack_w8", "moe_quant_rows_fp8",
     "moe_layer_workspace_bytes_w8a8", "moe_layer_forward_w8a8", "moe_gateup_swiglu_w8a8",
-    "moe_down_w8a8",
+    "moe_down_w8a8", "moe_debug_set_waits",
 )
 
 
@@ -101,6 +101,7 @@ def lib() -> ctypes.CDLL:
         "moe_layer_forward_w8a8": ([p, p, p, D, W8, W8, W8, W8, p, p, sz, p], i32),
         "moe_gateup_swiglu_w8a8": ([p, D, p, W8, W8, p, p, sz, p], i32),
         "moe_down_w8a8": ([p, D, W8, W8, p, p, sz, p], i32),
+        "moe_debug_set_waits": ([p, sz, ctypes.c_uint64, i32, p], i32),
         "moe_pack_w4_bytes": ([i64, i64, i32, ctypes.POINTER(sz)], sz),
         "moe_import_q4_blocks": ([p, i64, i64, i32, p, p, p, p], i32),
         "moe_combine_shared": ([p, p, p, D, p, p], i32),
@@ -226,6 +227,12 @@ def moe_down_w8a8(H, dims: Dims, Wd: W8, Wd_s: W8, Y, ws, stream=None):
     _check(lib().moe_down_w8a8(
         _dev(H, torch.int16, "H"), ctypes.byref(dims), Wd, Wd_s, _dev(Y, torch.float32, "Y"),
         _ptr(ws), ws.numel(), _stream(stream)), "moe_down_w8a8")
+
+
+def moe_debug_set_waits(ws, wait_ns: int, withhold_stage: int, stream=None):
+    """Test hook: the bounded waits' limit and a withheld pipeline stage (see moe.h)."""
+    _check(lib().moe_debug_set_waits(_ptr(ws), ws.numel(), wait_ns, withhold_stage,
+                                     _stream(stream)), "moe_debug_set_waits")
 
 
 def moe_import_q4_blocks(blocks: torch.Tensor, K: int, group: int, w_scratch=None,

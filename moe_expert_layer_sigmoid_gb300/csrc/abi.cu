@@ -143,6 +143,11 @@ namespace {
 
 moe_status_t map_err(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+__global__ void set_waits_kernel(WsHeader* hdr, unsigned long long wait_ns, int withhold_stage) {
+    hdr->wait_ns = wait_ns;
+    hdr->withhold_stage = withhold_stage;
+}
+
 moe_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
     if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(ws) % 256) return MOE_ERR_WORKSPACE;
@@ -603,6 +608,16 @@ moe_status_t moe_layer_forward_host(const uint16_t* x_host, const float* W_r, co
     if (cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
+}
+
+moe_status_t moe_debug_set_waits(void* ws, size_t ws_bytes, uint64_t wait_ns,
+                                 int32_t withhold_stage, void* stream) {
+    if (!ws || ws_bytes < sizeof(WsHeader) || reinterpret_cast<uintptr_t>(ws) % 256)
+        return MOE_ERR_WORKSPACE;
+    if (withhold_stage < 0) return MOE_ERR_INVALID_ARG;
+    set_waits_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<WsHeader*>(ws), (unsigned long long)wait_ns, withhold_stage);
+    return map_err(cudaGetLastError());
 }
 
 moe_status_t moe_check_device_status(void* ws, size_t ws_bytes, void* stream) {

@@ -42,21 +42,42 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: gives up after kWaitNs (or once another warp gave up), records
-// the failure in the workspace header and returns false.
+// The wait limit: the header's test setting, else kWaitNs.
+__device__ __forceinline__ uint64_t wait_limit(const WsHeader* hdr) {
+    const uint64_t v = hdr ? *reinterpret_cast<const volatile uint64_t*>(&hdr->wait_ns) : 0;
+    return v ? v : kWaitNs;
+}
+
+// Bounded wait: gives up after the wait limit (or once another warp gave up),
+// records the failure in the workspace header and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           WsHeader* hdr) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
+    const uint64_t limit = wait_limit(hdr);
     for (uint32_t i = 1;; ++i) {
         if (mbar_try(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitNs) {
+            if (globaltimer() - t0 > limit) {
                 *abort_flag = 1;
                 record_error(hdr, kErrWaitTimeout);
                 return false;
             }
+        }
+    }
+}
+
+// Teardown wait for this thread's own asynchronous work (copies or MMAs it
+// issued) after an abort: ignores the abort flag, still bounded by the limit.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, WsHeader* hdr) {
+    const uint64_t t0 = globaltimer();
+    const uint64_t limit = wait_limit(hdr);
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 255u) == 255u && globaltimer() - t0 > limit) {
+            record_error(hdr, kErrWaitTimeout);
+            return false;
         }
     }
 }

@@ -29,7 +29,11 @@ struct WsHeader {
     int32_t n_tiles[2];    // grouped-GEMM tile counts: [0] gate+up, [1] down
     int32_t done[4];       // arrival counters; [0]: CTAs of router_decode_kernel (the last resets it);
                            // [2..3]: the single-launch step's 64-bit grid-barrier arrival count
-    int32_t pad[56];
+    // test hook (moe_debug_set_waits); both 0 in normal use
+    uint64_t wait_ns;       // limit of every bounded mbarrier wait (0: the 2 s default)
+    int32_t withhold_stage; // s > 0: the gate+up grouped kernel's CTA 0 skips the copies of
+                            // its s-th pipeline stage, so the stage's consumers time out
+    int32_t pad[53];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 

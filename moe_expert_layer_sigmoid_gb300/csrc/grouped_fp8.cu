@@ -54,9 +54,11 @@ constexpr int kF8TmemCols = kF8Acc * kF8Tok;
 constexpr int kF8OffA = 0;
 constexpr int kF8OffB = kF8OffA + kF8Stages * kF8ABytes;
 constexpr int kF8OffBar = kF8OffB + kF8Stages * kF8BBytes;
-// FULL[stages], EMPTY[stages], AFULL[acc], AEMPTY[acc]
+// FULL[stages], EMPTY[stages], AFULL[acc], AEMPTY[acc], TD (committed by the MMA
+// thread after an abort, to wait for its MMAs in flight before TMEM is freed)
 constexpr int kF8BarFull = 0, kF8BarEmpty = kF8Stages, kF8BarAFull = 2 * kF8Stages,
-              kF8BarAEmpty = kF8BarAFull + kF8Acc, kF8NumBars = kF8BarAEmpty + kF8Acc;
+              kF8BarAEmpty = kF8BarAFull + kF8Acc, kF8BarTd = kF8BarAEmpty + kF8Acc,
+              kF8NumBars = kF8BarTd + 1;
 constexpr int kF8OffMisc = kF8OffBar + kF8NumBars * 8;
 constexpr int kF8Smem = kF8OffMisc + 16 + 1024;  // + alignment slack
 static_assert(kF8Smem <= 227 * 1024, "shared memory budget");
@@ -121,6 +123,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
             mbar_init(bar(kF8BarAFull + b), 1);
             mbar_init(bar(kF8BarAEmpty + b), kF8Warps - kF8EpiWarp0);
         }
+        mbar_init(bar(kF8BarTd), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -153,6 +156,11 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            // test hook: CTA 0 of a gate+up launch skips the copies of one stage
+            const int64_t withheld =
+                (gateup && blockIdx.x == 0)
+                    ? (int64_t)*reinterpret_cast<volatile int32_t*>(&p.hdr->withhold_stage) - 1
+                    : -1;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
                 const int4 t = __ldg(p.tiles + tile);
                 if (!tile_ok(p, t)) {
@@ -171,6 +179,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                         ok = false;
                         break;
                     }
+                    if ((int64_t)it == withheld) continue;  // its FULL phase never completes
                     mbar_expect_tx(bar(kF8BarFull + s), (uint32_t)(kF8ABytes + brows * kF8K));
                     const uint32_t adst = sbase + kF8OffA + s * kF8ABytes;
                     if (gateup)  // rows m = 32 * blk + 16 * gu + i
@@ -183,11 +192,11 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                                 bar(kF8BarFull + s));
                 }
             }
-            // do not leave with copies in flight
-            if (!ok)
-                for (uint32_t j = (it >= kF8Stages ? it - kF8Stages : 0); j < it; ++j)
-                    mbar_wait(bar(kF8BarFull + j % kF8Stages), (j / kF8Stages) & 1, abort_flag,
-                              p.hdr);
+            // do not leave with copies in flight: wait (bounded, whatever the abort flag)
+            // for the stages issued last; without an abort their phases are complete
+            for (uint32_t j = (it >= kF8Stages ? it - kF8Stages : 0); j < it; ++j)
+                if ((int64_t)j != withheld)
+                    mbar_drain(bar(kF8BarFull + j % kF8Stages), (j / kF8Stages) & 1, p.hdr);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -229,10 +238,11 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                 mma_commit(bar(kF8BarAFull + b));
                 ++tc;
             }
-            // the last commit has landed before the CTA can exit
-            if (ok && last >= 0)
-                mbar_wait(bar(kF8BarEmpty + last % kF8Stages), (uint32_t)(last / kF8Stages) & 1,
-                          abort_flag, p.hdr);
+            // the MMAs are done before the CTA frees TMEM: a commit of its own, waited
+            // for whatever the abort flag
+            (void)last;
+            mma_commit(bar(kF8BarTd));
+            mbar_drain(bar(kF8BarTd), 0, p.hdr);
         }
         __syncwarp();
     } else {

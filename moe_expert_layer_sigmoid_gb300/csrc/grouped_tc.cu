@@ -101,7 +101,9 @@ constexpr int kOffBar = kOffSc + 2 * kScBytes;
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAReady = 2 * kStages,
               kBarDFull = kBarAReady + kAStagesT,
               kBarDEmpty = kBarDFull + kDBufs, kBarScFull = kBarDEmpty + kDBufs,
-              kBarScEmpty = kBarScFull + 2, kNumBars = kBarScEmpty + 2;
+              kBarScEmpty = kBarScFull + 2, kBarTd = kBarScEmpty + 2, kNumBars = kBarTd + 2;
+// TD[2]: one per MMA issuer, committed after an abort so the issuer can wait for
+// its MMAs in flight before the CTA frees TMEM.
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -231,6 +233,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kBarScFull + b), 1);
             mbar_init(bar(kBarScEmpty + b), kEpilogueWarps);
+            mbar_init(bar(kBarTd + b), 1);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -264,7 +267,12 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
             if (lane == 0) {
                 uint32_t it = 0;
                 bool ok = true;
-                int tc = 0;
+                int tc = 0, sc_issued = 0;
+                // test hook: CTA 0 of a gate+up launch skips the copies of one stage
+                const int64_t withheld =
+                    (p.mode == kGateUp && blockIdx.x == 0)
+                        ? (int64_t)*reinterpret_cast<volatile int32_t*>(&p.hdr->withhold_stage) - 1
+                        : -1;
                 int4 cur = load_tile(p, blockIdx.x, n_tiles);
                 for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid, ++tc) {
                     const int4 nxt = load_tile(p, tile + grid, n_tiles);  // one tile ahead
@@ -290,12 +298,14 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                         bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, bytes,
                                   bar(kBarScFull + sb));
                     }
+                    ++sc_issued;
                     const CUtensorMap* tma = ti.grp >= 0 ? &p.tm_a : &p.tm_a_sh;
                     const int nks = ti.K / kKStage;
                     for (int ks = 0; ks < nks; ++ks, ++it) {
                         const int s = it % kStages;
                         const uint32_t ph = (it / kStages) & 1;
                         if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1, abort_flag, p.hdr)) { ok = false; break; }
+                        if ((int64_t)it == withheld) continue;  // its FULL phase never completes
                         const int brows = b_box_rows(ti.npad);
                         mbar_expect_tx(bar(kBarFull + s), (uint32_t)(kAStageBytes + brows * 256));
                         // one box each: the weight tile and both 64-wide K blocks of the activations
@@ -311,10 +321,14 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     }
                     cur = nxt;
                 }
-                // do not leave with copies in flight
-                if (!ok)
-                    for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j)
-                        mbar_wait(bar(kBarFull + j % kStages), (j / kStages) & 1, abort_flag, p.hdr);
+                // do not leave with copies in flight: wait (bounded, whatever the abort
+                // flag) for the stages and scale blocks issued last.  In a run that did
+                // not abort their phases are complete and each test passes at once.
+                for (uint32_t j = (it >= kStages ? it - kStages : 0); j < it; ++j)
+                    if ((int64_t)j != withheld)
+                        mbar_drain(bar(kBarFull + j % kStages), (j / kStages) & 1, p.hdr);
+                for (int t = sc_issued > 2 ? sc_issued - 2 : 0; t < sc_issued; ++t)
+                    mbar_drain(bar(kBarScFull + (t & 1)), (t >> 1) & 1, p.hdr);
             }
             __syncwarp();
         } else if (warp == 1 || warp == 2) {
@@ -379,9 +393,11 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     }
                     cur = nxt;
                 }
-                // this issuer's last commit has landed before the CTA can exit
-                if (ok && last >= 0)
-                    mbar_wait(bar(kBarEmpty + last % kStages), (uint32_t)(last / kStages) & 1, abort_flag, p.hdr);
+                // this issuer's MMAs are done before the CTA frees TMEM: a commit of its
+                // own, waited for whatever the abort flag
+                (void)last;
+                mma_commit(bar(kBarTd + me));
+                mbar_drain(bar(kBarTd + me), 0, p.hdr);
             }
             __syncwarp();
         }

@@ -235,3 +235,10 @@ def test_w8a8_entries_validate_before_launch(L):
                                     ok, ws, need, None) == INV
     assert L.moe_layer_forward_w8a8(ok + 8, ok, ok, ctypes.byref(d), w8, w8, w8, w8, ok, ws, need,
                                     None) == INV
+
+
+def test_debug_set_waits_validation(L):
+    assert L.moe_debug_set_waits(None, 1 << 20, 0, 0, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_debug_set_waits(256 + 8, 1 << 20, 0, 0, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_debug_set_waits(1 << 20, 16, 0, 0, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_debug_set_waits(1 << 20, 1 << 20, 0, -1, None) == moe.MOE_ERR_INVALID_ARG
