@@ -35,6 +35,8 @@ WsLayout ws_layout(const moe_dims_t& d) {
     off += align256(sizeof(uint16_t) * (size_t)(rows * d.d));
     L.hist = off;
     off += align256(sizeof(int32_t) * (size_t)desc_blocks(slots) * (size_t)E);
+    L.wr_planes = off;
+    if (T > kRouterSmallT && router_tc_supported(d)) off += align256(sizeof(uint16_t) * 3 * (size_t)E * d.d);
     L.step_bytes = off;
 
     L.topk_idx = off;
@@ -270,7 +272,8 @@ moe_status_t layer_forward(const uint16_t* x, const float* W_r, const float* bia
             if (e != cudaSuccess) return MOE_ERR_CUDA;
         } else {
             e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
-                              ws_at<float>(ws, L.logits), L.router_ksplit, L.router_ksplit_large, s);
+                              ws_at<float>(ws, L.logits), L.router_ksplit, L.router_ksplit_large,
+                              ws_at<uint16_t>(ws, L.wr_planes), hdr, s);
             if (e != cudaSuccess) return MOE_ERR_CUDA;
             e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
                                    ws_at<int4>(ws, L.tiles), L.max_tiles,
@@ -290,7 +293,8 @@ moe_status_t layer_forward(const uint16_t* x, const float* W_r, const float* bia
                                         pos, residual, out, hdr, true, s));
     }
     e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr, ws_at<float>(ws, L.logits),
-                      L.router_ksplit, L.router_ksplit_large, s);
+                      L.router_ksplit, L.router_ksplit_large, ws_at<uint16_t>(ws, L.wr_planes), hdr,
+                      s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_descriptors(topk_idx, d, counts, offsets, perm, pos, sched, hdr,
                            ws_at<int4>(ws, L.tiles), L.max_tiles, ws_at<int32_t>(ws, L.hist), s);
@@ -374,7 +378,8 @@ moe_status_t moe_router_topk(const uint16_t* x, const float* W_r, const float* b
     if (!act_ok(x) || !act_ok(W_r) || !bias || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
     return map_err(launch_router(x, W_r, bias, *dims, topk_idx, topk_w, margin,
                                  ws_at<float>(ws, L.logits), L.router_ksplit,
-                                 L.router_ksplit_large, static_cast<cudaStream_t>(stream)));
+                                 L.router_ksplit_large, ws_at<uint16_t>(ws, L.wr_planes),
+                                 ws_at<WsHeader>(ws, L.header), static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_build_descriptors(const int32_t* topk_idx, const moe_dims_t* dims,
@@ -572,7 +577,7 @@ moe_status_t moe_layer_forward_w8a8(const uint16_t* x, const float* W_r, const f
     const int4* tiles = ws_at<int4>(ws, L.tiles);
     cudaError_t e = launch_router(x, W_r, bias, d, topk_idx, topk_w, nullptr,
                                   ws_at<float>(ws, L.logits), L.router_ksplit,
-                                  L.router_ksplit_large, s);
+                                  L.router_ksplit_large, ws_at<uint16_t>(ws, L.wr_planes), hdr, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_descriptors(topk_idx, d, ws_at<int32_t>(ws, L.counts), ws_at<int32_t>(ws, L.offsets),
                            perm, pos, ws_at<int32_t>(ws, L.sched), hdr, ws_at<int4>(ws, L.tiles),

@@ -50,6 +50,7 @@ struct WsLayout {
     size_t tiles;         // int4 tile descriptors of the grouped kernels
     size_t xs;            // bf16 [T*k + T][d] gathered activation rows (grouped path)
     size_t hist;          // int32 [desc_blocks(T*k)][E] descriptor-sort histograms
+    size_t wr_planes;     // bf16 [3][E][d] router weight planes (tensor-core router, T > 64)
     size_t step_bytes;
     // whole-layer workspace (moe_layer_workspace_bytes) adds the intermediates
     size_t topk_idx, topk_w, counts, offsets, perm, pos, sched, H, Y, x_stage, out_stage;
@@ -128,11 +129,19 @@ cudaError_t launch_import_q4_direct(const uint8_t* blocks, int64_t rows, int64_t
                                     float* w, uint8_t* q, uint16_t* s, cudaStream_t st);
 
 // Router: logits as split-K partials (ksplit slices for T <= kRouterSmallT,
-// ksplit_large above it), then the top-k.
+// ksplit_large above it), then the top-k.  Above kRouterSmallT the logits run
+// on the tensor cores (router_tc.cu) when `planes` (workspace for the bf16
+// split of W_r) is given and the shape allows, else as an fp32 SGEMM.
 int router_ksplit_large(const moe_dims_t& d);
 cudaError_t launch_router(const uint16_t* x, const float* W_r, const float* bias,
                           const moe_dims_t& d, int32_t* topk_idx, float* topk_w, float* margin,
-                          float* logits, int ksplit, int ksplit_large, cudaStream_t st);
+                          float* logits, int ksplit, int ksplit_large, uint16_t* planes,
+                          WsHeader* hdr, cudaStream_t st);
+bool router_tc_supported(const moe_dims_t& d);
+int router_tc_ksplit(const moe_dims_t& d);
+cudaError_t launch_router_logits_tc(const uint16_t* x, const float* W_r, const moe_dims_t& d,
+                                    uint16_t* planes, float* logits, int ks, WsHeader* hdr,
+                                    cudaStream_t st);
 
 // `hist` is workspace of desc_blocks(T * k) * E int32 (per-block histograms).
 int desc_blocks(int64_t nslots);

@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(256) router_topk(const float* __restrict__ par
 }  // namespace
 
 int router_ksplit_large(const moe_dims_t& d) {
+    if (router_tc_supported(d)) return router_tc_ksplit(d);
     const int64_t tiles = (int64_t)((d.T + kSgBM - 1) / kSgBM) * ((d.E + kSgBN - 1) / kSgBN);
     int ks = 1;
     while (ks * 2 <= d.d / 256 && tiles * ks * 2 <= 320) ks *= 2;
@@ -149,13 +150,18 @@ int router_ksplit_large(const moe_dims_t& d) {
 
 cudaError_t launch_router(const uint16_t* x, const float* W_r, const float* bias,
                           const moe_dims_t& dm, int32_t* topk_idx, float* topk_w, float* margin,
-                          float* logits, int ksplit, int ksplit_large, cudaStream_t st) {
+                          float* logits, int ksplit, int ksplit_large, uint16_t* planes,
+                          WsHeader* hdr, cudaStream_t st) {
     const int T = dm.T, d = dm.d, E = dm.E, k = dm.k;
     int ks = 1;
     if (T <= kRouterSmallT) {
         ks = ksplit;  // d / ks is 256 or 512
         dim3 grid((E + 7) / 8, ks);
         router_logits_gemv<<<grid, 256, 0, st>>>(x, W_r, T, d, E, d / ks, logits);
+    } else if (planes && router_tc_supported(dm)) {
+        ks = ksplit_large;
+        cudaError_t e = launch_router_logits_tc(x, W_r, dm, planes, logits, ks, hdr, st);
+        if (e != cudaSuccess) return e;
     } else {
         ks = ksplit_large;  // a power of two dividing d / 256
         dim3 grid((E + kSgBN - 1) / kSgBN, (T + kSgBM - 1) / kSgBM, ks);

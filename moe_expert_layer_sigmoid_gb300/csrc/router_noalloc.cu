@@ -68,6 +68,7 @@ extern "C" moe_status_t moe_router_topk_noalloc(const uint16_t* x, const float* 
     // The logits kernel writes every partial that the top-k kernel reads within
     // this call, so leftovers of an earlier call never leak into the result.
     cudaError_t err = moe::launch_router(x, W_r, bias, *dims, topk_idx, topk_w, margin, scratch,
-                                         L.router_ksplit, 1, static_cast<cudaStream_t>(stream));
+                                         L.router_ksplit, 1, nullptr, nullptr,
+                                         static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

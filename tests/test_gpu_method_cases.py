@@ -58,9 +58,10 @@ def _tie_bias(E: int, k: int, seed: int) -> np.ndarray:
 
 # ------------------------------------------------------------------ router ties
 
-TIE_ROUTER = [  # (T, d, E, k): the T = 1, T <= 8, T <= 64 and prefill forms
+TIE_ROUTER = [  # (T, d, E, k): the T = 1, T <= 8, T <= 64 and prefill forms (fp32 SGEMM at
+    # E = 64, the tensor-core form at E = 256)
     (1, 4096, 256, 10), (5, 1024, 64, 6), (8, 512, 16, 4), (40, 4096, 256, 10),
-    (300, 1024, 64, 8),
+    (300, 1024, 64, 8), (300, 1024, 256, 8),
 ]
 
 
