@@ -68,6 +68,10 @@ WsLayout ws_layout(const moe_dims_t& d) {
     off += align256((size_t)(rows * Fmax));
     L.w8_ha = off;
     off += align256(sizeof(float) * (size_t)rows);
+    L.w8_xt = off;
+    off += align256((size_t)(T * d.d));
+    L.w8_xta = off;
+    off += align256(sizeof(float) * (size_t)T);
     L.w8a8_bytes = off;
     return L;
 }
@@ -534,6 +538,7 @@ moe_status_t moe_gateup_swiglu_w8a8(const uint16_t* x, const moe_dims_t* dims,
     return map_err(launch_gateup_w8a8(x, *dims, perm, Wgu, Wgu_s, H, ws_at<WsHeader>(ws, L.header),
                                       ws_at<int4>(ws, L.tiles), L.max_tiles,
                                       ws_at<uint8_t>(ws, L.xs), ws_at<float>(ws, L.w8_xa),
+                                      ws_at<uint8_t>(ws, L.w8_xt), ws_at<float>(ws, L.w8_xta),
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -579,12 +584,14 @@ moe_status_t moe_layer_forward_w8a8(const uint16_t* x, const float* W_r, const f
                                   ws_at<float>(ws, L.logits), L.router_ksplit,
                                   L.router_ksplit_large, ws_at<uint16_t>(ws, L.wr_planes), hdr, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    // 256-token tiles: the fp8 kernel goes faster with more flops per weight byte
     e = launch_descriptors(topk_idx, d, ws_at<int32_t>(ws, L.counts), ws_at<int32_t>(ws, L.offsets),
                            perm, pos, ws_at<int32_t>(ws, L.sched), hdr, ws_at<int4>(ws, L.tiles),
-                           L.max_tiles, ws_at<int32_t>(ws, L.hist), s);
+                           L.max_tiles, ws_at<int32_t>(ws, L.hist), s, 256);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_gateup_w8a8(x, d, perm, Wgu, Wgu_s, H, hdr, tiles, L.max_tiles,
-                           ws_at<uint8_t>(ws, L.xs), ws_at<float>(ws, L.w8_xa), s);
+                           ws_at<uint8_t>(ws, L.xs), ws_at<float>(ws, L.w8_xa),
+                           ws_at<uint8_t>(ws, L.w8_xt), ws_at<float>(ws, L.w8_xta), s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_down_w8a8(H, d, Wd, Wd_s, Y, hdr, tiles + L.max_tiles, L.max_tiles,
                          ws_at<uint8_t>(ws, L.w8_hq), ws_at<float>(ws, L.w8_ha), s);

@@ -58,6 +58,7 @@ struct WsLayout {
     // W8A8 layer (moe_layer_workspace_bytes_w8a8) adds the fp8 operands; the
     // gate+up codes [T*k + T][d] reuse the xs region
     size_t w8_xa, w8_hq, w8_ha;  // x row scales, H codes [T*k + T][max(F, F_s)], H row scales
+    size_t w8_xt, w8_xta;        // each token's x codes [T][d] and scale [T]
     size_t w8a8_bytes;
     int router_ksplit;    // K split of the small-T router
     int router_ksplit_large;  // K split of the large-T router
@@ -145,10 +146,11 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const float* W_r, const m
 
 // `hist` is workspace of desc_blocks(T * k) * E int32 (per-block histograms).
 int desc_blocks(int64_t nslots);
+// `tile_n`: tokens per tile of the tile lists (128; 256 for the W8A8 kernel).
 cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int32_t* counts,
                                int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,
                                WsHeader* hdr, int4* tiles, int64_t max_tiles, int32_t* hist,
-                               cudaStream_t st);
+                               cudaStream_t st, int tile_n = kTileN);
 
 // Decode expert GEMVs (experts_gemv.cu).  `n_active` is the count of routed
 // groups with rows (the workspace header's, written by the fused router) or
@@ -193,10 +195,12 @@ cudaError_t launch_down_grouped(const uint16_t* H, const moe_dims_t& d, moe_w4_t
 bool w8a8_supported(const moe_dims_t& d);
 cudaError_t launch_quant_rows_fp8(const void* src, bool bf16, int64_t rows, int64_t K, uint8_t* q,
                                   float* s, cudaStream_t st);
+// The gate+up launch quantises each token's x once (xt, xta: [T][d], [T]), then
+// copies the codes into descriptor order (xq, a).
 cudaError_t launch_gateup_w8a8(const uint16_t* x, const moe_dims_t& d, const int32_t* perm,
                                moe_w8_t Wgu, moe_w8_t Wgu_s, uint16_t* H, WsHeader* hdr,
                                const int4* tiles, int64_t max_tiles, uint8_t* xq, float* a,
-                               cudaStream_t st);
+                               uint8_t* xt, float* xta, cudaStream_t st);
 cudaError_t launch_down_w8a8(const uint16_t* H, const moe_dims_t& d, moe_w8_t Wd, moe_w8_t Wd_s,
                              float* Y, WsHeader* hdr, const int4* tiles, int64_t max_tiles,
                              uint8_t* hq, float* a, cudaStream_t st);

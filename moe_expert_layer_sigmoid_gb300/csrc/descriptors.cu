@@ -111,8 +111,8 @@ desc_place(const int32_t* __restrict__ topk_idx, int64_t nslots, int E,
 
 constexpr int kScatterThreads = 256;
 
-// Tile schedule of the grouped tcgen05 kernels.  A token tile is up to 128
-// consecutive rows of one group (routed expert or the shared expert); a tile
+// Tile schedule of the grouped tcgen05 kernels.  A token tile is up to tn (128,
+// or 256 for the W8A8 kernel) consecutive rows of one group (routed expert or the shared expert); a tile
 // pairs it with one weight band (gate+up: 64 gate rows and their 64 up rows;
 // down: 128 output channels).  Groups run largest first: the shared expert,
 // then the routed experts in schedule order.  Within a group the order is
@@ -120,15 +120,15 @@ constexpr int kScatterThreads = 256;
 // read the same weight band (L2 reuse); with MOE_FLAG_NO_SCHED groups go in
 // expert-id order and tiles token-tile-major.
 struct TileGeom {
-    int T, k, nb_gu_routed, nb_gu_shared, nb_dn;
+    int T, k, nb_gu_routed, nb_gu_shared, nb_dn, tn;
     bool sched;
     int64_t max_tiles;
 };
 
 __device__ __forceinline__ void write_group_tiles(int4* tiles, int list, int64_t base, int grp,
-                                                  int row0, int count, int nb, bool banded,
+                                                  int row0, int count, int nb, bool banded, int tn,
                                                   int64_t max_tiles, WsHeader* hdr) {
-    const int ntt = (count + 127) / 128;
+    const int ntt = (count + tn - 1) / tn;
     for (int i = threadIdx.x; i < ntt * nb; i += blockDim.x) {
         const int band = banded ? i / ntt : i % nb;
         const int tt = banded ? i % ntt : i / nb;
@@ -138,7 +138,7 @@ __device__ __forceinline__ void write_group_tiles(int4* tiles, int list, int64_t
             continue;
         }
         tiles[list * max_tiles + idx] =
-            make_int4(grp, row0 + 128 * tt, min(128, count - 128 * tt), band);
+            make_int4(grp, row0 + tn * tt, min(tn, count - tn * tt), band);
     }
 }
 
@@ -156,7 +156,7 @@ desc_plan(int64_t nslots, int E, const int32_t* __restrict__ counts, int32_t* __
     for (int e2 = tid; e2 < E; e2 += kScatterThreads) {
         const int c2 = counts[e2];
         const bool before = c2 > my_count || (c2 == my_count && e2 < e);
-        const int ntt2 = (c2 + 127) / 128;
+        const int ntt2 = (c2 + tg.tn - 1) / tg.tn;
         if (e2 < e) off += c2;
         if (before) ++rank;
         if (tg.sched ? before : e2 < e) tt_before += ntt2;
@@ -207,11 +207,12 @@ desc_plan(int64_t nslots, int E, const int32_t* __restrict__ counts, int32_t* __
     }
     __syncthreads();
     const int base_row = red[0][0];
-    const int ntt_sh = (tg.T + 127) / 128;
+    const int ntt_sh = (tg.T + tg.tn - 1) / tg.tn;
     if (shared_cta) {
         const int row0 = (int)nslots;
-        write_group_tiles(tiles, 0, 0, -1, row0, tg.T, tg.nb_gu_shared, tg.sched, tg.max_tiles, hdr);
-        write_group_tiles(tiles, 1, 0, -1, row0, tg.T, tg.nb_dn, tg.sched, tg.max_tiles, hdr);
+        write_group_tiles(tiles, 0, 0, -1, row0, tg.T, tg.nb_gu_shared, tg.sched, tg.tn, tg.max_tiles,
+                          hdr);
+        write_group_tiles(tiles, 1, 0, -1, row0, tg.T, tg.nb_dn, tg.sched, tg.tn, tg.max_tiles, hdr);
         if (tid == 0 && hdr) {
             const int ta = red[4][0];
             hdr->n_tiles[0] = ntt_sh * tg.nb_gu_shared + ta * tg.nb_gu_routed;
@@ -222,9 +223,9 @@ desc_plan(int64_t nslots, int E, const int32_t* __restrict__ counts, int32_t* __
     if (my_count > 0) {
         const int tb = red[3][0];
         write_group_tiles(tiles, 0, (int64_t)ntt_sh * tg.nb_gu_shared + (int64_t)tb * tg.nb_gu_routed,
-                          e, base_row, my_count, tg.nb_gu_routed, tg.sched, tg.max_tiles, hdr);
+                          e, base_row, my_count, tg.nb_gu_routed, tg.sched, tg.tn, tg.max_tiles, hdr);
         write_group_tiles(tiles, 1, (int64_t)(ntt_sh + tb) * tg.nb_dn, e, base_row, my_count,
-                          tg.nb_dn, tg.sched, tg.max_tiles, hdr);
+                          tg.nb_dn, tg.sched, tg.tn, tg.max_tiles, hdr);
     }
 }
 
@@ -235,7 +236,7 @@ int desc_blocks(int64_t nslots) { return (int)((nslots + kDescSlots - 1) / kDesc
 cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int32_t* counts,
                                int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,
                                WsHeader* hdr, int4* tiles, int64_t max_tiles, int32_t* hist,
-                               cudaStream_t st) {
+                               cudaStream_t st, int tile_n) {
     const int64_t nslots = (int64_t)d.T * d.k;
     const int nblk = desc_blocks(nslots);
     const size_t hist_smem = sizeof(int) * (size_t)d.E;
@@ -256,6 +257,7 @@ cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int
     tg.nb_dn = d.d / 128;
     tg.sched = !(d.flags & MOE_FLAG_NO_SCHED);
     tg.max_tiles = max_tiles;
+    tg.tn = tile_n;
     desc_plan<<<d.E + 1, kScatterThreads, 0, st>>>(nslots, d.E, counts, offsets, sched, hdr, tiles, tg);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (nblk > 0) {

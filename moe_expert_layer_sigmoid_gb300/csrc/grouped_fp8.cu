@@ -18,17 +18,20 @@
 // e4m3(x / a), both divisions in fp32.  Each product of two codes is exact; a
 // projection is v = (acc * a) * s_w with acc the fp32 sum over K.
 //
-// Tiles are the W4A16 grouped path's (the descriptors build both lists): M =
-// 128 weight rows (gate+up: 64 gate rows and their 64 up rows interleaved in
-// blocks of 16, so a gate row and its up row are 16 lanes apart in one warp;
-// down: 128 output channels), N = up to 128 tokens of one expert, K in stages
-// of 128 bytes.  Per stage one TMA box of weight codes (128 x 128 B) and one
-// of activation codes (128 rows x 128 B), both with 128-byte swizzle, the
-// UMMA K-major canonical layout; four MMAs of K = 32 per stage.
+// Tiles come from the descriptors, as on the W4A16 grouped path but with up to
+// 256 tokens: M = 128 weight rows (gate+up: 64 gate rows and their 64 up rows
+// interleaved in blocks of 16, so a gate row and its up row are 16 lanes apart
+// in one warp; down: 128 output channels), N = up to 256 tokens of one expert,
+// K in stages of 128 bytes.  Per stage one TMA box of weight codes (128 x 128
+// B) and one of activation codes (32, 64, 128 or 256 rows x 128 B, the
+// smallest that holds the tile's tokens), both with 128-byte swizzle, the UMMA
+// K-major canonical layout; four MMAs of K = 32 per stage.  The kernel is
+// bound by the bytes each SM has in flight over their latency, so 256-token
+// tiles (twice the flops per weight byte of 128-token ones) go faster.
 //
 // Warp roles (6 warps, one CTA per SM): warp 0 TMA producer; warp 1 allocates
 // TMEM and issues the MMAs; warps 2-5 the epilogue (each reads the 32 TMEM
-// lanes of its quarter).  Two 128-column accumulators let the epilogue of one
+// lanes of its quarter).  Two 256-column accumulators let the epilogue of one
 // tile overlap the MMAs of the next.
 #include <cuda.h>
 #include <cuda_fp8.h>
@@ -43,9 +46,9 @@ namespace {
 constexpr int kF8Warps = 6;
 constexpr int kF8Threads = kF8Warps * 32;
 constexpr int kF8EpiWarp0 = 2;
-constexpr int kF8Stages = 6;
+constexpr int kF8Stages = 4;
 constexpr int kF8K = 128;                    // K bytes (= elements) per stage
-constexpr int kF8Tok = 128;                  // tokens (N) per tile at most
+constexpr int kF8Tok = 256;                  // tokens (N) per tile at most
 constexpr int kF8ABytes = 128 * kF8K;        // weight codes of a stage
 constexpr int kF8BBytes = kF8Tok * kF8K;     // activation codes of a stage
 constexpr int kF8Acc = 2;                    // accumulator buffers in TMEM
@@ -69,6 +72,7 @@ struct F8Params {
     CUtensorMap tm_b;        // activation codes [rows][K] bytes, box {128, 128}
     CUtensorMap tm_b32;      // box {128, 32}: tiles of at most 32 tokens
     CUtensorMap tm_b64;      // box {128, 64}: tiles of 33-64 tokens
+    CUtensorMap tm_b256;     // box {128, 256}: tiles of 129-256 tokens
     CUtensorMap tm_a;        // routed weight codes (gate+up 5D, down 2D)
     CUtensorMap tm_a_sh;     // shared-expert weight codes, same boxes
     const float* s_routed;   // weight row scales [E * rows_per_expert]
@@ -88,7 +92,7 @@ struct F8Params {
 // rows holding its npad tokens (the MMA reads npad rows).
 __device__ __forceinline__ int f8_box_rows(int n) {
     const int npad = (n + 15) & ~15;
-    return npad <= 32 ? 32 : npad <= 64 ? 64 : 128;
+    return npad <= 32 ? 32 : npad <= 64 ? 64 : npad <= 128 ? 128 : 256;
 }
 
 // A tile the descriptors could have written: a group id in [-1, E), 1..128
@@ -133,6 +137,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
         prefetch_tmap(&p.tm_b);
         prefetch_tmap(&p.tm_b32);
         prefetch_tmap(&p.tm_b64);
+        prefetch_tmap(&p.tm_b256);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -170,7 +175,10 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                 const int grp = t.x, row0 = t.y, band = t.w;
                 const CUtensorMap* tma = grp >= 0 ? &p.tm_a : &p.tm_a_sh;
                 const int brows = f8_box_rows(t.z);
-                const CUtensorMap* tmb = brows == 32 ? &p.tm_b32 : brows == 64 ? &p.tm_b64 : &p.tm_b;
+                const CUtensorMap* tmb = brows == 32    ? &p.tm_b32
+                                         : brows == 64  ? &p.tm_b64
+                                         : brows == 128 ? &p.tm_b
+                                                        : &p.tm_b256;
                 const int nks = tile_K(grp) / kF8K;
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     const int s = it % kF8Stages;
@@ -373,17 +381,22 @@ __device__ __forceinline__ void quant_row(const Src* src, int cols, uint8_t* dst
     }
 }
 
-// Gate+up operand: row r < T*k is slot perm[r]'s token, row T*k + t token t.
-__global__ void __launch_bounds__(256) quant_gather_x_kernel(const uint16_t* __restrict__ x,
-                                                             const int32_t* __restrict__ perm,
-                                                             int T, int k, int d,
-                                                             uint8_t* __restrict__ xq,
-                                                             float* __restrict__ a) {
+// Gate+up operand in descriptor order, from each token's codes: row r < T*k is
+// slot perm[r]'s token, row T*k + t token t.  One warp per row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_codes_kernel(const uint8_t* __restrict__ xt,
+                                                           const float* __restrict__ xta,
+                                                           const int32_t* __restrict__ perm,
+                                                           int T, int k, int d,
+                                                           uint8_t* __restrict__ xq,
+                                                           float* __restrict__ a) {
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t slots = (int64_t)T * k;
     if (r >= slots + T) return;
     const int64_t t = r < slots ? __ldg(perm + r) / k : r - slots;
-    quant_row<uint16_t>(x + t * d, d, xq + r * d, a + r, threadIdx.x & 31);
+    const uint4* src = reinterpret_cast<const uint4*>(xt + t * d);
+    uint4* dst = reinterpret_cast<uint4*>(xq + r * d);
+    for (int c = threadIdx.x & 31; c < d / 16; c += 32) dst[c] = __ldg(src + c);
+    if ((threadIdx.x & 31) == 0) a[r] = __ldg(xta + t);
 }
 
 // Down operand: H rows [T*k + T][ld] (routed rows F columns, shared rows F_s).
@@ -459,17 +472,19 @@ cudaError_t launch_quant_rows_fp8(const void* src, bool bf16, int64_t rows, int6
 cudaError_t launch_gateup_w8a8(const uint16_t* x, const moe_dims_t& d, const int32_t* perm,
                                moe_w8_t Wgu, moe_w8_t Wgu_s, uint16_t* H, WsHeader* hdr,
                                const int4* tiles, int64_t max_tiles, uint8_t* xq, float* a,
-                               cudaStream_t st) {
+                               uint8_t* xt, float* xta, cudaStream_t st) {
     const int64_t rows = (int64_t)d.T * d.k + d.T;
-    quant_gather_x_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(x, perm, d.T, d.k, d.d, xq,
-                                                                      a);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_quant_rows_fp8(x, true, d.T, d.d, xt, xta, st);
     if (err != cudaSuccess) return err;
+    gather_codes_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(xt, xta, perm, d.T, d.k, d.d,
+                                                                    xq, a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     F8Params prm;
     memset(&prm, 0, sizeof(prm));
     if (!make_codes_map(&prm.tm_b, xq, d.d, rows, d.d) ||
         !make_codes_map(&prm.tm_b32, xq, d.d, rows, d.d, 32) ||
         !make_codes_map(&prm.tm_b64, xq, d.d, rows, d.d, 64) ||
+        !make_codes_map(&prm.tm_b256, xq, d.d, rows, d.d, 256) ||
         !make_gateup_codes_map(&prm.tm_a, Wgu.q, d.d, d.F, d.E) ||
         !make_gateup_codes_map(&prm.tm_a_sh, Wgu_s.q, d.d, d.F_s, 1))
         return cudaErrorInvalidValue;
@@ -501,6 +516,7 @@ cudaError_t launch_down_w8a8(const uint16_t* H, const moe_dims_t& d, moe_w8_t Wd
     if (!make_codes_map(&prm.tm_b, hq, Fmax, rows, Fmax) ||
         !make_codes_map(&prm.tm_b32, hq, Fmax, rows, Fmax, 32) ||
         !make_codes_map(&prm.tm_b64, hq, Fmax, rows, Fmax, 64) ||
+        !make_codes_map(&prm.tm_b256, hq, Fmax, rows, Fmax, 256) ||
         !make_codes_map(&prm.tm_a, Wd.q, d.F, (uint64_t)d.E * d.d, d.F) ||
         !make_codes_map(&prm.tm_a_sh, Wd_s.q, d.F_s, (uint64_t)d.d, d.F_s))
         return cudaErrorInvalidValue;
