@@ -18,7 +18,7 @@ WsLayout ws_layout(const moe_dims_t& d) {
     L.router_ksplit = (d.d % 512 == 0) ? d.d / 512 : d.d / 256;
     L.router_ksplit_large = router_ksplit_large(d);
     const int64_t ks = T <= kRouterSmallT ? L.router_ksplit : L.router_ksplit_large;
-    // tile lists: one entry per (group, 128-row weight band, 128-token tile)
+    // tile lists: one entry per (group, 128-row weight band, token tile of up to kTileN)
     const int64_t groups = std::min<int64_t>(E, slots) + 1;
     const int64_t tok_tiles = (slots + kTileN - 1) / kTileN + groups + (T + kTileN - 1) / kTileN;
     const int64_t bands = (std::max<int64_t>(d.d, 2 * Fmax) + kTileM - 1) / kTileM;

@@ -108,7 +108,7 @@ constexpr int kMaxExperts = 1024;
 
 // Grouped-GEMM tile geometry (weight rows x tokens).
 constexpr int kTileM = 128;
-constexpr int kTileN = 128;
+constexpr int kTileN = 192;
 
 WsLayout ws_layout(const moe_dims_t& d);
 
@@ -146,7 +146,7 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const float* W_r, const m
 
 // `hist` is workspace of desc_blocks(T * k) * E int32 (per-block histograms).
 int desc_blocks(int64_t nslots);
-// `tile_n`: tokens per tile of the tile lists (128; 256 for the W8A8 kernel).
+// `tile_n`: tokens per tile of the tile lists (192; 256 for the W8A8 kernel).
 cudaError_t launch_descriptors(const int32_t* topk_idx, const moe_dims_t& d, int32_t* counts,
                                int32_t* offsets, int32_t* perm, int32_t* pos, int32_t* sched,
                                WsHeader* hdr, int4* tiles, int64_t max_tiles, int32_t* hist,
@@ -227,6 +227,15 @@ __device__ __forceinline__ float bf16_hi(uint32_t pair) {
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
     __nv_bfloat16 b = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// SwiGLU of one gate / up pair in fp32: silu(g) * u with silu(g) = g / (1 + e^-g).
+// The exponential and the division are the hardware approximations (__expf,
+// __fdividef): a few fp32 ulp from the correctly rounded forms, far below the
+// bf16 rounding that H gets next.  Every expert path uses this one form.
+// Limits: g -> -inf gives -0 (e^-g = inf), g -> +inf gives g * u.
+__device__ __forceinline__ float swiglu_f32(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // a0 += s * v0, a1 += s * v1 as one packed f32x2 FMA (sm_100 family); each

@@ -604,7 +604,7 @@ __device__ __noinline__ void gu_reduce(const TcGuArgs& a, bool shared, int64_t r
         const int y = (int)(rb / nfb);
         const int f = (int)(rb - (int64_t)y * nfb) * 8 + tile_row(gg);
         const int hr = shared ? a.T * a.k : srow[y];
-        a.H[(int64_t)hr * a.ldh + f] = float_to_bf16_bits(sg / (1.0f + expf(-sg)) * su);
+        a.H[(int64_t)hr * a.ldh + f] = float_to_bf16_bits(swiglu_f32(sg, su));
     }
     __syncthreads();
 }

@@ -184,7 +184,7 @@ __device__ __forceinline__ void load_chunk(const uint16_t* row, int c, uint4* xv
     for (int v = 0; v < 4; ++v) xv[v] = __ldg(p + v);
 }
 
-__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+__device__ __forceinline__ float swiglu(float g, float u) { return swiglu_f32(g, u); }
 
 // ---------------------------------------------------------------------------
 constexpr size_t kMaxStagedH = 64 * 1024;  // H rows staged by the down kernel, at most

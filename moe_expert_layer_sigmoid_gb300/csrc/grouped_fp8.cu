@@ -302,7 +302,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                             const float gv = lo ? val : other;
                             const float uv = lo ? other : val;
                             if (lo == (j < 16) && nn < n) {
-                                const float hv = gv / (1.0f + expf(-gv)) * uv;
+                                const float hv = swiglu_f32(gv, uv);
                                 reinterpret_cast<uint16_t*>(p.out)[(int64_t)(row0 + nn) * p.ld_out + col] =
                                     float_to_bf16_bits(hv);
                             }

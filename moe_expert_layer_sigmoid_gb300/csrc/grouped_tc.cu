@@ -9,13 +9,16 @@
 // mma.sync code for GB10; this one is written for sm_103a.
 //
 // Shape of one tile: M = 128 weight rows (swap-AB: weights take the M slot),
-// N = up to 128 tokens of one expert (rounded up to 16), K = the full
-// contraction in stages of 128.  A gate+up tile holds 64 gate rows and the 64
+// N = up to 192 tokens of one expert (rounded up to 16), K = the full
+// contraction in stages of 128.  192 is the widest N for which two A stages and
+// two accumulators fit in the 512 TMEM columns; against 128-token tiles it cuts
+// the MMA instructions per flop by a third, and the dequantisation passes over
+// each weight tile (one per token tile) by up to a third.  A gate+up tile holds 64 gate rows and the 64
 // matching up rows, interleaved in blocks of 16 (gate f..f+15, up f..f+15,
 // ...), so a gate row and its up row sit 16 lanes apart in the same warp and
 // SwiGLU is finished with one shuffle.
 //
-// Activation rows are read as plain 128-row TMA boxes: the down projection
+// Activation rows are read as plain TMA boxes of up to 192 rows: the down projection
 // reads H, whose rows are already grouped by expert; gate+up reads x gathered
 // once into that same row order (gather_rows_kernel), which replaces per-row
 // gathers inside the GEMM that the TMA unit serves slowly.
@@ -32,8 +35,8 @@
 //   warps 4-11  dequantisers, two per TMEM lane quarter (warps 4-7 the first
 //               64 K of a stage, 8-11 the second): int4 -> bf16 integers
 //               (exact), tcgen05.st to TMEM
-//   warps 12-19 epilogue, two per lane quarter (warps 12-15 columns 0-31 and
-//               64-95, 16-19 columns 32-63 and 96-127): per group, read the
+//   warps 12-19 epilogue, two per lane quarter (warps 12-15 the 32-column
+//               blocks 0, 2, 4; warps 16-19 blocks 1, 3, 5): per group, read the
 //               group's partial sums from TMEM and accumulate s * partial in
 //               fp32 registers (packed f32x2 FMAs); at the end of a tile apply
 //               SwiGLU (gate+up) or store Y (down)
@@ -48,8 +51,8 @@
 // Numerics: each group's partial sum is sum_k x_k * q_k with exact bf16
 // products and fp32 accumulation; multiplying by the fp16 scale s in fp32
 // gives sum_k x_k * (q_k * s), the dequantised product, without rounding the
-// weights.  TMEM: two A stages at columns [0, 128), three 128-column
-// accumulators at [128, 512), so the MMAs can run two groups ahead of the
+// weights.  TMEM: two A stages at columns [0, 128), two 192-column
+// accumulators at [128, 512), so the MMAs can run one group ahead of the
 // epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -72,21 +75,23 @@ constexpr int kEpilogueWarps = 8;
 // dequantisers (4-11), epilogue (12-19).  Their sum over the CTA must not
 // exceed what the launch holds (checked on the host before every launch:
 // a setmaxnreg.inc that cannot be served would wait forever).
-constexpr int kRegCtl = 32, kRegDq = 72, kRegEpi = 152;
+constexpr int kRegCtl = 40, kRegDq = 56, kRegEpi = 160;
 constexpr int kRegBudget = 128 * (kRegCtl + 2 * kRegDq + 2 * kRegEpi);
 static_assert(kRegBudget <= 65536, "register split exceeds the register file");
-constexpr int kStages = 5;                        // shared-memory pipeline depth
+constexpr int kStages = 3;                        // shared-memory pipeline depth
 constexpr int kAStagesT = 2;                      // A operand stages in TMEM
-constexpr int kDBufs = 3;                         // accumulator buffers in TMEM
+constexpr int kDBufs = 2;                         // accumulator buffers in TMEM
 static_assert(kAStagesT < kStages, "dequant reuses the stage barrier of the MMA it waits for");
 constexpr int kKStage = 128;                      // K elements per stage
-constexpr int kTokTile = 128;                     // max tokens (N) per tile
+constexpr int kTokTile = 192;                     // max tokens (N) per tile
 constexpr int kBStageBytes = 2 * kTokTile * 128;  // two 64-wide K blocks, 128 B per row
 constexpr int kAStageBytes = 128 * 64;            // 128 rows x 64 bytes of nibbles
 constexpr int kMaxGroupsPerRow = 32;              // scale buffer capacity (K / group)
 constexpr int kScBytes = 128 * kMaxGroupsPerRow * 2;
 constexpr int kTmemCols = 512;
 constexpr int kTmemD = kAStagesT * 64;            // first accumulator column
+static_assert(kTmemD + kDBufs * kTokTile <= 512, "A stages and accumulators exceed the TMEM columns");
+static_assert(kTokTile == kTileN, "the descriptors' tile lists use kTileN tokens per tile");
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffB = 0;
@@ -112,9 +117,10 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 enum Mode : int { kGateUp = 0, kDown = 1 };
 
 struct GroupedParams {
-    CUtensorMap tm_b;        // activation rows (gathered x or H), bf16, box {64, 128}, 128B swizzle
+    CUtensorMap tm_b;        // activation rows (gathered x or H), bf16, box {64, 192}, 128B swizzle
     CUtensorMap tm_b32;      // the same rows, box {64, 32}: tiles of at most 32 tokens
     CUtensorMap tm_b64;      // box {64, 64}: tiles of 33-64 tokens
+    CUtensorMap tm_b128;     // box {64, 128}: tiles of 65-128 tokens
     CUtensorMap tm_a;        // routed int4 weights, uint8 rows; gate+up box {64, 16}, down {64, 128}
     CUtensorMap tm_a_sh;     // shared-expert int4 weights, same boxes
     const __half* s_routed;  // [E * rows_per_expert][K / group]
@@ -183,10 +189,12 @@ __device__ __forceinline__ TileInfo decode_tile(const GroupedParams& p, int4 t) 
     return ti;
 }
 
-// Activation rows one stage loads for a tile: the smallest box of 32, 64 or 128
-// rows that holds its npad tokens (the MMA reads npad rows; smaller boxes keep
-// small-token tiles from moving 128 rows per stage).
-__device__ __forceinline__ int b_box_rows(int npad) { return npad <= 32 ? 32 : npad <= 64 ? 64 : 128; }
+// Activation rows one stage loads for a tile: the smallest box of 32, 64, 128 or
+// 192 rows that holds its npad tokens (the MMA reads npad rows; smaller boxes
+// keep small-token tiles from moving 192 rows per stage).
+__device__ __forceinline__ int b_box_rows(int npad) {
+    return npad <= 32 ? 32 : npad <= 64 ? 64 : npad <= 128 ? 128 : 192;
+}
 
 __device__ __forceinline__ int4 load_tile(const GroupedParams& p, int tile, int n_tiles) {
     return tile < n_tiles ? __ldg(p.tiles + tile) : make_int4(0, 0, 1, 0);
@@ -244,6 +252,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_b)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_b32)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_b64)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_b128)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -316,7 +325,11 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                         else
                             tma_load_2d(adst, tma, ks * 64, weight_row(p, ti, 0, 0), bar(kBarFull + s));
                         tma_load_3d(sbase + kOffB + s * kBStageBytes,
-                                    brows == 32 ? &p.tm_b32 : brows == 64 ? &p.tm_b64 : &p.tm_b, 0, ti.row0, 2 * ks,
+                                    brows == 32    ? &p.tm_b32
+                                    : brows == 64  ? &p.tm_b64
+                                    : brows == 128 ? &p.tm_b128
+                                                   : &p.tm_b,
+                                    0, ti.row0, 2 * ks,
                                     bar(kBarFull + s));
                     }
                     cur = nxt;
@@ -377,7 +390,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t dcol = tmem + (uint32_t)(kTmemD + b * 128);
+                            const uint32_t dcol = tmem + (uint32_t)(kTmemD + b * kTokTile);
     #pragma unroll
                             for (int kk = 0; kk < G / 16; ++kk) {
                                 const int kg = gg * (G / 16) + kk;  // 16-wide K step within the stage
@@ -471,10 +484,10 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         const int q = warp & 3;
         const int half = (warp - kEpilogueWarp0) >> 2;
         const int m = q * 32 + lane;
-        // 32-column blocks half and half + 2, so both warps of a quarter have work
-        // when a tile holds 33-96 tokens: acc[j] is column col(j)
-        const int col0 = half * 32;
-        auto col = [&](int j) { return j < 32 ? col0 + j : 64 + col0 + (j - 32); };
+        // the 32-column blocks half, half + 2, half + 4, so both warps of a quarter
+        // have work whenever a tile holds more than 32 tokens: acc[j] is column col(j)
+        constexpr int kEpiCols = kTokTile / 2;
+        auto col = [&](int j) { return 32 * (2 * (j >> 5) + half) + (j & 31); };
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         // gate+up: row m is gate (gu = 0) or up (gu = 1) row f_local of the band
         const int gu = (m >> 4) & 1;
@@ -490,29 +503,26 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
             if (ok && !mbar_wait(bar(kBarScFull + sb), (tc >> 1) & 1, abort_flag, p.hdr)) ok = false;
             const __half* sc = reinterpret_cast<const __half*>(smem + kOffSc + sb * kScBytes);
             const __half* srow = p.mode == kGateUp ? sc + (gu * 64 + f_local) * ti.ng : sc + m * ti.ng;
-            float acc[64];
+            float acc[kEpiCols];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+            for (int j = 0; j < kEpiCols; ++j) acc[j] = 0.f;
             for (int g = 0; g < ti.ng; ++g, ++gi) {
                 const int b = gi % kDBufs;
                 if (ok && !mbar_wait(bar(kBarDFull + b), (gi / kDBufs) & 1, abort_flag, p.hdr)) ok = false;
                 if (!ok) continue;
                 tc_fence_after();
                 const float s = __half2float(srow[g]);
-                const uint32_t dcol = tmem + lane_base + (uint32_t)(kTmemD + b * 128 + col0);
-                if (col0 < ti.npad) {
-                    uint32_t v[64];
-                    const bool two = 64 + col0 < ti.npad;
-                    tmem_ld_x32(dcol, v);
-                    if (two) tmem_ld_x32(dcol + 64, v + 32);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                const uint32_t dcol = tmem + lane_base + (uint32_t)(kTmemD + b * kTokTile);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2)
-                        ffma2(acc[j], acc[j + 1], s, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-                    if (two) {
+                for (int blk = 0; blk < kEpiCols / 32; ++blk) {
+                    const int c0 = 32 * (2 * blk + half);
+                    if (c0 < ti.npad) {
+                        uint32_t v[32];
+                        tmem_ld_x32(dcol + (uint32_t)c0, v);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                        for (int j = 32; j < 64; j += 2)
-                            ffma2(acc[j], acc[j + 1], s, __uint_as_float(v[j]),
+                        for (int j = 0; j < 32; j += 2)
+                            ffma2(acc[32 * blk + j], acc[32 * blk + j + 1], s, __uint_as_float(v[j]),
                                   __uint_as_float(v[j + 1]));
                     }
                 }
@@ -523,26 +533,26 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(bar(kBarScEmpty + sb));
             if (p.mode == kGateUp) {
-                // lane i holds gate row f, lane i ^ 16 the up row of the same f;
-                // the gate lanes store the first 32 of the warp's tokens, the up lanes the rest
-                uint16_t* H = reinterpret_cast<uint16_t*>(p.out);
-                const int f = 64 * ti.band + f_local;
+                // lane i holds gate row f, lane i ^ 16 the up row of the same f.  Step j
+                // finishes column col(j) on the gate lanes and column col(j + kEpiCols / 2)
+                // on the up lanes: each lane sends the value its partner needs, so every
+                // lane computes one SwiGLU per step
+                uint16_t* H = reinterpret_cast<uint16_t*>(p.out) + 64 * ti.band + f_local;
                 const bool lo = (lane & 16) == 0;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float other = __shfl_xor_sync(0xffffffffu, acc[j], 16);
-                    const float gv = lo ? acc[j] : other;
-                    const float uv = lo ? other : acc[j];
-                    const int nn = col(j);
-                    if (ok && lo == (j < 32) && nn < ti.n) {
-                        const float hv = gv / (1.0f + expf(-gv)) * uv;
-                        H[(int64_t)(ti.row0 + nn) * p.ld_out + f] = float_to_bf16_bits(hv);
-                    }
+                for (int j = 0; j < kEpiCols / 2; ++j) {
+                    const float mine = lo ? acc[j] : acc[j + kEpiCols / 2];
+                    const float other = __shfl_xor_sync(0xffffffffu, lo ? acc[j + kEpiCols / 2] : acc[j], 16);
+                    const float gv = lo ? mine : other;
+                    const float uv = lo ? other : mine;
+                    const int nn = col(lo ? j : j + kEpiCols / 2);
+                    if (ok && nn < ti.n)
+                        H[(int64_t)(ti.row0 + nn) * p.ld_out] = float_to_bf16_bits(swiglu_f32(gv, uv));
                 }
             } else if (ok) {
                 float* Y = reinterpret_cast<float*>(p.out);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
+                for (int j = 0; j < kEpiCols; ++j) {
                     const int nn = col(j);
                     if (nn < ti.n) Y[(int64_t)(ti.row0 + nn) * p.ld_out + 128 * ti.band + m] = acc[j];
                 }
@@ -631,6 +641,7 @@ bool make_act_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows
 
 bool make_act_maps(GroupedParams& prm, const void* base, uint64_t cols, uint64_t rows) {
     return make_act_map(&prm.tm_b, base, cols, rows, kTokTile) &&
+           make_act_map(&prm.tm_b128, base, cols, rows, 128) &&
            make_act_map(&prm.tm_b32, base, cols, rows, 32) &&
            make_act_map(&prm.tm_b64, base, cols, rows, 64);
 }
