@@ -176,7 +176,7 @@ struct TileInfo {
     int ng;     // quantisation groups along K
 };
 
-template <int G>
+template <int G, int MODE>
 __device__ __forceinline__ TileInfo decode_tile(const GroupedParams& p, int4 t) {
     TileInfo ti;
     ti.grp = t.x;
@@ -184,7 +184,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GroupedParams& p, int4 t) 
     ti.n = t.z;
     ti.band = t.w;
     ti.npad = (t.z + 15) & ~15;
-    ti.K = p.mode == kGateUp ? p.d : (t.x >= 0 ? p.F : p.Fs);
+    ti.K = MODE == kGateUp ? p.d : (t.x >= 0 ? p.F : p.Fs);
     ti.ng = ti.K / G;
     return ti;
 }
@@ -202,9 +202,10 @@ __device__ __forceinline__ int4 load_tile(const GroupedParams& p, int tile, int 
 
 // First weight row (within the routed or shared weight tensor) of the tile's
 // block of rows: gate+up block (gu, blk) = 16 rows; down = the 128 rows.
+template <int MODE>
 __device__ __forceinline__ int weight_row(const GroupedParams& p, const TileInfo& ti, int gu,
                                           int blk) {
-    if (p.mode == kGateUp) {
+    if (MODE == kGateUp) {
         const int Fg = ti.grp >= 0 ? p.F : p.Fs;
         const int base = ti.grp >= 0 ? ti.grp * 2 * p.F : 0;
         return base + gu * Fg + 64 * ti.band + 16 * blk;
@@ -213,7 +214,9 @@ __device__ __forceinline__ int weight_row(const GroupedParams& p, const TileInfo
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int G>  // quantisation group size along K
+// G: quantisation group size along K; MODE: kGateUp or kDown (one instantiation
+// each, so each gets its own register allocation).
+template <int G, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -265,7 +268,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int n_tiles = *reinterpret_cast<volatile int*>(&p.hdr->n_tiles[p.mode]);
+    const int n_tiles = *reinterpret_cast<volatile int*>(&p.hdr->n_tiles[MODE]);
     const int grid = gridDim.x;
 
     if (warp < kDequantWarp0) {
@@ -279,13 +282,13 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 int tc = 0, sc_issued = 0;
                 // test hook: CTA 0 of a gate+up launch skips the copies of one stage
                 const int64_t withheld =
-                    (p.mode == kGateUp && blockIdx.x == 0)
+                    (MODE == kGateUp && blockIdx.x == 0)
                         ? (int64_t)*reinterpret_cast<volatile int32_t*>(&p.hdr->withhold_stage) - 1
                         : -1;
                 int4 cur = load_tile(p, blockIdx.x, n_tiles);
                 for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid, ++tc) {
                     const int4 nxt = load_tile(p, tile + grid, n_tiles);  // one tile ahead
-                    const TileInfo ti = decode_tile<G>(p, cur);
+                    const TileInfo ti = decode_tile<G, MODE>(p, cur);
                     // the tile's scale block(s)
                     const int sb = tc & 1;
                     if (!mbar_wait(bar(kBarScEmpty + sb), ((tc >> 1) & 1) ^ 1, abort_flag, p.hdr)) {
@@ -294,17 +297,17 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     }
                     const __half* sbase_g = ti.grp >= 0 ? p.s_routed : p.s_shared;
                     const uint32_t scdst = sbase + kOffSc + sb * kScBytes;
-                    if (p.mode == kGateUp) {
+                    if (MODE == kGateUp) {
                         const uint32_t blk_bytes = 64u * ti.ng * 2u;
                         mbar_expect_tx(bar(kBarScFull + sb), 2 * blk_bytes);
-                        bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, blk_bytes,
+                        bulk_load(scdst, sbase_g + (int64_t)weight_row<MODE>(p, ti, 0, 0) * ti.ng, blk_bytes,
                                   bar(kBarScFull + sb));
-                        bulk_load(scdst + blk_bytes, sbase_g + (int64_t)weight_row(p, ti, 1, 0) * ti.ng,
+                        bulk_load(scdst + blk_bytes, sbase_g + (int64_t)weight_row<MODE>(p, ti, 1, 0) * ti.ng,
                                   blk_bytes, bar(kBarScFull + sb));
                     } else {
                         const uint32_t bytes = 128u * ti.ng * 2u;
                         mbar_expect_tx(bar(kBarScFull + sb), bytes);
-                        bulk_load(scdst, sbase_g + (int64_t)weight_row(p, ti, 0, 0) * ti.ng, bytes,
+                        bulk_load(scdst, sbase_g + (int64_t)weight_row<MODE>(p, ti, 0, 0) * ti.ng, bytes,
                                   bar(kBarScFull + sb));
                     }
                     ++sc_issued;
@@ -319,11 +322,11 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                         mbar_expect_tx(bar(kBarFull + s), (uint32_t)(kAStageBytes + brows * 256));
                         // one box each: the weight tile and both 64-wide K blocks of the activations
                         const uint32_t adst = sbase + kOffA + s * kAStageBytes;
-                        if (p.mode == kGateUp)  // rows m = 32*blk + 16*gu + i (gate/up interleaved)
+                        if (MODE == kGateUp)  // rows m = 32*blk + 16*gu + i (gate/up interleaved)
                             tma_load_5d(adst, tma, ks * 64, 0, 0, 4 * ti.band, ti.grp >= 0 ? ti.grp : 0,
                                         bar(kBarFull + s));
                         else
-                            tma_load_2d(adst, tma, ks * 64, weight_row(p, ti, 0, 0), bar(kBarFull + s));
+                            tma_load_2d(adst, tma, ks * 64, weight_row<MODE>(p, ti, 0, 0), bar(kBarFull + s));
                         tma_load_3d(sbase + kOffB + s * kBStageBytes,
                                     brows == 32    ? &p.tm_b32
                                     : brows == 64  ? &p.tm_b64
@@ -358,7 +361,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 int4 cur = load_tile(p, blockIdx.x, n_tiles);
                 for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
                     const int4 nxt = load_tile(p, tile + grid, n_tiles);
-                    const TileInfo ti = decode_tile<G>(p, cur);
+                    const TileInfo ti = decode_tile<G, MODE>(p, cur);
                     const uint32_t idesc = idesc_bf16(128, ti.npad);
                     // 16-byte units between the stage's two 64-wide K blocks of B
                     const int kb_units = b_box_rows(ti.npad) * 8;
@@ -426,7 +429,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         int4 cur = load_tile(p, blockIdx.x, n_tiles);
         for (int tile = blockIdx.x; tile < n_tiles && ok; tile += grid) {
             const int4 nxt = load_tile(p, tile + grid, n_tiles);
-            const TileInfo ti = decode_tile<G>(p, cur);
+            const TileInfo ti = decode_tile<G, MODE>(p, cur);
             const int nks = ti.K / kKStage;
             for (int ks = 0; ks < nks; ++ks, ++it) {
                 const int s = it % kStages;
@@ -442,7 +445,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarEmpty + s));
                 uint32_t r[32];
-                if (p.mode == kGateUp) {  // activations stored block-permuted
+                if (MODE == kGateUp) {  // activations stored block-permuted
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         nib8_to_bf16x2_paired(v[c].x, r + 16 * c + 0);
@@ -498,11 +501,11 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         int4 cur = load_tile(p, blockIdx.x, n_tiles);
         for (int tile = blockIdx.x; tile < n_tiles; tile += grid, ++tc) {
             const int4 nxt = load_tile(p, tile + grid, n_tiles);
-            const TileInfo ti = decode_tile<G>(p, cur);
+            const TileInfo ti = decode_tile<G, MODE>(p, cur);
             const int sb = tc & 1;
             if (ok && !mbar_wait(bar(kBarScFull + sb), (tc >> 1) & 1, abort_flag, p.hdr)) ok = false;
             const __half* sc = reinterpret_cast<const __half*>(smem + kOffSc + sb * kScBytes);
-            const __half* srow = p.mode == kGateUp ? sc + (gu * 64 + f_local) * ti.ng : sc + m * ti.ng;
+            const __half* srow = MODE == kGateUp ? sc + (gu * 64 + f_local) * ti.ng : sc + m * ti.ng;
             float acc[kEpiCols];
 #pragma unroll
             for (int j = 0; j < kEpiCols; ++j) acc[j] = 0.f;
@@ -513,26 +516,34 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 tc_fence_after();
                 const float s = __half2float(srow[g]);
                 const uint32_t dcol = tmem + lane_base + (uint32_t)(kTmemD + b * kTokTile);
+                // the accumulator is released as soon as the warp's last block of it is
+                // in registers, before that block's FMAs
 #pragma unroll
                 for (int blk = 0; blk < kEpiCols / 32; ++blk) {
                     const int c0 = 32 * (2 * blk + half);
+                    const bool last = blk == kEpiCols / 32 - 1 || c0 + 64 >= ti.npad;
+                    uint32_t v[32];
                     if (c0 < ti.npad) {
-                        uint32_t v[32];
                         tmem_ld_x32(dcol + (uint32_t)c0, v);
                         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    }
+                    if (last) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(kBarDEmpty + b));
+                    }
+                    if (c0 < ti.npad) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 2)
                             ffma2(acc[32 * blk + j], acc[32 * blk + j + 1], s, __uint_as_float(v[j]),
                                   __uint_as_float(v[j + 1]));
                     }
+                    if (last) break;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarDEmpty + b));
             }
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(bar(kBarScEmpty + sb));
-            if (p.mode == kGateUp) {
+            if (MODE == kGateUp) {
                 // lane i holds gate row f, lane i ^ 16 the up row of the same f.  Step j
                 // finishes column col(j) on the gate lanes and column col(j + kEpiCols / 2)
                 // on the up lanes: each lane sends the value its partner needs, so every
@@ -674,21 +685,26 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
     return r == CUDA_SUCCESS;
 }
 
-template <int G>
-cudaError_t launch_g(GroupedParams& prm, int sms, cudaStream_t st) {
-    cudaError_t err = ensure_dynamic_smem((const void*)grouped_w4a16_kernel<G>, kSmemBytes);
+template <int G, int MODE>
+cudaError_t launch_gm(GroupedParams& prm, int sms, cudaStream_t st) {
+    cudaError_t err = ensure_dynamic_smem((const void*)grouped_w4a16_kernel<G, MODE>, kSmemBytes);
     if (err != cudaSuccess) return err;
     // the warpgroups' setmaxnreg targets must fit in the registers the launch holds
     static int launch_regs = -1;
     if (launch_regs < 0) {
         cudaFuncAttributes fa;
-        err = cudaFuncGetAttributes(&fa, grouped_w4a16_kernel<G>);
+        err = cudaFuncGetAttributes(&fa, grouped_w4a16_kernel<G, MODE>);
         if (err != cudaSuccess) return err;
         launch_regs = fa.numRegs;
     }
     if (launch_regs * kThreads < kRegBudget) return cudaErrorInvalidConfiguration;
-    grouped_w4a16_kernel<G><<<sms, kThreads, kSmemBytes, st>>>(prm);
+    grouped_w4a16_kernel<G, MODE><<<sms, kThreads, kSmemBytes, st>>>(prm);
     return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_g(GroupedParams& prm, int sms, cudaStream_t st) {
+    return prm.mode == kGateUp ? launch_gm<G, kGateUp>(prm, sms, st) : launch_gm<G, kDown>(prm, sms, st);
 }
 
 cudaError_t launch(GroupedParams& prm, cudaStream_t st) {
