@@ -24,7 +24,7 @@
 // gathers inside the GEMM that the TMA unit serves slowly.
 //
 // Warp roles (20 warps, one CTA per SM; setmaxnreg moves registers from the
-// control warpgroup to the epilogue's):
+// control and dequantiser warpgroups to the epilogue's):
 //   warp 0      TMA producer: per tile the fp16 scale block (bulk copy), per
 //               stage the int4 weight tile (64B swizzle) and the activation
 //               tile (128B swizzle, the UMMA K-major canonical layout)
@@ -32,21 +32,23 @@
 //               kind::f16, A from TMEM, B from shared memory, fp32 accumulator
 //               in TMEM; even quantisation groups on warp 1, odd on warp 2
 //   warp 3      idle
-//   warps 4-11  dequantisers, two per TMEM lane quarter (warps 4-7 the first
-//               64 K of a stage, 8-11 the second): int4 -> bf16 integers
-//               (exact), tcgen05.st to TMEM
-//   warps 12-19 epilogue, two per lane quarter (warps 12-15 the 32-column
-//               blocks 0, 2, 4; warps 16-19 blocks 1, 3, 5): per group, read the
-//               group's partial sums from TMEM and accumulate s * partial in
-//               fp32 registers (packed f32x2 FMAs); at the end of a tile apply
+//   warps 4-7   dequantisers, one per TMEM lane quarter, the stage's full K:
+//               int4 -> bf16 integers (exact), tcgen05.st to TMEM
+//   warps 8-19  epilogue, three per lane quarter (warp part p takes the
+//               32-column blocks p and p + 3): per group, read the group's
+//               partial sums from TMEM and accumulate s * partial in fp32
+//               registers (packed f32x2 FMAs); at the end of a tile apply
 //               SwiGLU (gate+up) or store Y (down)
 //
-// Two dequantisers per quarter keep the conversion ahead of the MMAs (one
-// took ~900 cycles per stage, latency-bound, against ~550 of tensor time).
-// Two MMA issuers on two schedulers hide each other's barrier and commit
-// latency; each TMEM A slot is used by every second stage, so splitting the
-// stages by parity gives every AREADY barrier a single waiter that consumes its
-// phases in order (a parity wait cannot tell phase k from phase k - 2).
+// The per-group drain of the accumulators is the loop that sets the stage
+// period (MMA -> commit -> epilogue reads -> accumulator free -> next MMA), so
+// the epilogue gets three warps per quarter (two TMEM round trips per group
+// and warp instead of three) and the dequantisers, which convert before they
+// wait for their TMEM slot, one.  Two MMA issuers on two schedulers hide each
+// other's barrier and commit latency; each TMEM A slot is used by every second
+// stage, so splitting the stages by parity gives every AREADY barrier a single
+// waiter that consumes its phases in order (a parity wait cannot tell phase k
+// from phase k - 2).
 //
 // Numerics: each group's partial sum is sum_k x_k * q_k with exact bf16
 // products and fp32 accumulation; multiplying by the fp16 scale s in fp32
@@ -65,18 +67,20 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = 20;
+constexpr int kWarps = 20;  // control warpgroup + dequantisers + epilogue
 constexpr int kThreads = kWarps * 32;
+constexpr int kDqPerQuarter = 1;    // dequantiser warps per TMEM lane quarter
+constexpr int kEpiPerQuarter = 3;   // epilogue warps per TMEM lane quarter
 constexpr int kDequantWarp0 = 4;
-constexpr int kDequantWarps = 8;
-constexpr int kEpilogueWarp0 = 12;
-constexpr int kEpilogueWarps = 8;
+constexpr int kDequantWarps = 4 * kDqPerQuarter;
+constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantWarps;
+constexpr int kEpilogueWarps = 4 * kEpiPerQuarter;
 // Registers per thread after setmaxnreg: control warpgroup (warps 0-3),
 // dequantisers (4-11), epilogue (12-19).  Their sum over the CTA must not
 // exceed what the launch holds (checked on the host before every launch:
 // a setmaxnreg.inc that cannot be served would wait forever).
-constexpr int kRegCtl = 40, kRegDq = 56, kRegEpi = 160;
-constexpr int kRegBudget = 128 * (kRegCtl + 2 * kRegDq + 2 * kRegEpi);
+constexpr int kRegCtl = 40, kRegDq = 80, kRegEpi = 120;
+constexpr int kRegBudget = 128 * (kRegCtl + kDqPerQuarter * kRegDq + kEpiPerQuarter * kRegEpi);
 static_assert(kRegBudget <= 65536, "register split exceeds the register file");
 constexpr int kStages = 3;                        // shared-memory pipeline depth
 constexpr int kAStagesT = 2;                      // A operand stages in TMEM
@@ -421,7 +425,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         // ------------------------------------------------------------ dequantisers
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegDq));
         const int q = warp & 3;
-        const int h = (warp - kDequantWarp0) >> 2;  // which 64 K of the stage
+        const int h = (warp - kDequantWarp0) >> 2;  // which part of the stage's K
+        constexpr int kChunks = 4 / kDqPerQuarter;  // 16-byte chunks (32 K each) per warp
         const int m = q * 32 + lane;  // tile row = TMEM lane
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t it = 0;
@@ -436,18 +441,18 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 const uint32_t ph = (it / kStages) & 1;
                 if (!mbar_wait(bar(kBarFull + s), ph, abort_flag, p.hdr)) { ok = false; break; }
                 // row m of the int4 tile: 64 bytes, 16-byte chunks 64B-swizzled by the TMA;
-                // this warp's half is chunks 2h and 2h + 1
+                // this warp's part is chunks kChunks * h .. kChunks * h + kChunks - 1
                 const uint8_t* arow = smem + kOffA + s * kAStageBytes + m * 64;
-                uint4 v[2];
+                uint4 v[kChunks];
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    v[c] = *reinterpret_cast<const uint4*>(arow + (((2 * h + c) ^ ((m >> 1) & 3)) << 4));
+                for (int c = 0; c < kChunks; ++c)
+                    v[c] = *reinterpret_cast<const uint4*>(arow + (((kChunks * h + c) ^ ((m >> 1) & 3)) << 4));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarEmpty + s));
-                uint32_t r[32];
+                uint32_t r[16 * kChunks];
                 if (MODE == kGateUp) {  // activations stored block-permuted
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < kChunks; ++c) {
                         nib8_to_bf16x2_paired(v[c].x, r + 16 * c + 0);
                         nib8_to_bf16x2_paired(v[c].y, r + 16 * c + 4);
                         nib8_to_bf16x2_paired(v[c].z, r + 16 * c + 8);
@@ -455,7 +460,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < kChunks; ++c) {
                         nib8_to_bf16x2(v[c].x, r + 16 * c + 0);
                         nib8_to_bf16x2(v[c].y, r + 16 * c + 4);
                         nib8_to_bf16x2(v[c].z, r + 16 * c + 8);
@@ -471,7 +476,9 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                     }
                 }
                 tc_fence_after();
-                tmem_st_x32(tmem + lane_base + (uint32_t)(ta * 64 + 32 * h), r);
+#pragma unroll
+                for (int c2 = 0; c2 < kChunks / 2; ++c2)
+                    tmem_st_x32(tmem + lane_base + (uint32_t)(ta * 64 + 32 * (h * kChunks / 2 + c2)), r + 32 * c2);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
@@ -485,12 +492,14 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         // After a failed wait every epilogue warp keeps walking the same tiles
         // (skipping the work), so no warp waits on a barrier the others left.
         const int q = warp & 3;
-        const int half = (warp - kEpilogueWarp0) >> 2;
+        const int part = (warp - kEpilogueWarp0) >> 2;  // which of the quarter's epilogue warps
         const int m = q * 32 + lane;
-        // the 32-column blocks half, half + 2, half + 4, so both warps of a quarter
-        // have work whenever a tile holds more than 32 tokens: acc[j] is column col(j)
-        constexpr int kEpiCols = kTokTile / 2;
-        auto col = [&](int j) { return 32 * (2 * (j >> 5) + half) + (j & 31); };
+        // the 32-column blocks part, part + kEpiPerQuarter, ..., so every warp of a
+        // quarter has work whenever a tile holds more than 32 * (kEpiPerQuarter - 1)
+        // tokens: acc[j] is column col(j)
+        constexpr int kEpiCols = kTokTile / kEpiPerQuarter;
+        static_assert(kEpiCols % 32 == 0, "whole 32-column blocks per epilogue warp");
+        auto col = [&](int j) { return 32 * (kEpiPerQuarter * (j >> 5) + part) + (j & 31); };
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         // gate+up: row m is gate (gu = 0) or up (gu = 1) row f_local of the band
         const int gu = (m >> 4) & 1;
@@ -520,8 +529,8 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 // in registers, before that block's FMAs
 #pragma unroll
                 for (int blk = 0; blk < kEpiCols / 32; ++blk) {
-                    const int c0 = 32 * (2 * blk + half);
-                    const bool last = blk == kEpiCols / 32 - 1 || c0 + 64 >= ti.npad;
+                    const int c0 = 32 * (kEpiPerQuarter * blk + part);
+                    const bool last = blk == kEpiCols / 32 - 1 || c0 + 32 * kEpiPerQuarter >= ti.npad;
                     uint32_t v[32];
                     if (c0 < ti.npad) {
                         tmem_ld_x32(dcol + (uint32_t)c0, v);
