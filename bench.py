@@ -380,7 +380,7 @@ class GpuBench:
 # router_decode_kernel, gateup_gemv_kernel and down_gemv_kernel of one step, from
 # one `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` capture of this
 # code (cold caches, --ncopy 1 --nbatch 1, one step of three launches).
-DECODE1_TRAFFIC = 4_269_312 + 48_285_696 + 23_853_824
+DECODE1_TRAFFIC = 4_269_312 + 48_596_992 + 23_854_848
 
 
 def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
@@ -411,7 +411,7 @@ def gpu_roofline_decode(cfg, ms, active, pk, pk_kind, gu_ms, flags=0):
 
 # DRAM bytes (read + write) of one gate+up launch at prefill2048 from one
 # `ncu --set full` capture of grouped_w4a16_kernel on this code (cold caches).
-PREFILL2048_GATEUP_TRAFFIC = 363_650_816 + 46_725_120
+PREFILL2048_GATEUP_TRAFFIC = 356_328_704 + 47_281_664
 
 
 def gpu_roofline_prefill(cfg, gu_ms, pk, pk_kind):
