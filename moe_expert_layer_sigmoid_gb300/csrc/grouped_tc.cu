@@ -39,12 +39,16 @@
 //               partial sums from TMEM and accumulate s * partial in fp32
 //               registers (packed f32x2 FMAs); at the end of a tile apply
 //               SwiGLU (gate+up) or store Y (down)
+// Launches of at most 64 tokens use the other layout (Layout<2>): warps 4-11
+// dequantise (two per quarter, half of a stage's K each) and warps 12-19 are
+// the epilogue (two per quarter, blocks p, p + 2, p + 4).
 //
-// The per-group drain of the accumulators is the loop that sets the stage
-// period (MMA -> commit -> epilogue reads -> accumulator free -> next MMA), so
-// the epilogue gets three warps per quarter (two TMEM round trips per group
-// and warp instead of three) and the dequantisers, which convert before they
-// wait for their TMEM slot, one.  Two MMA issuers on two schedulers hide each
+// With many tokens per tile the per-group drain of the accumulators is the
+// loop that sets the stage period (MMA -> commit -> epilogue reads ->
+// accumulator free -> next MMA), so the epilogue gets three warps per quarter
+// (two TMEM round trips per group and warp instead of three) and the
+// dequantisers, which convert before they wait for their TMEM slot, one.  With
+// few tokens the conversion, paid per stage whatever the token count, sets it.  Two MMA issuers on two schedulers hide each
 // other's barrier and commit latency; each TMEM A slot is used by every second
 // stage, so splitting the stages by parity gives every AREADY barrier a single
 // waiter that consumes its phases in order (a parity wait cannot tell phase k
@@ -69,19 +73,28 @@ namespace {
 
 constexpr int kWarps = 20;  // control warpgroup + dequantisers + epilogue
 constexpr int kThreads = kWarps * 32;
-constexpr int kDqPerQuarter = 1;    // dequantiser warps per TMEM lane quarter
-constexpr int kEpiPerQuarter = 3;   // epilogue warps per TMEM lane quarter
 constexpr int kDequantWarp0 = 4;
-constexpr int kDequantWarps = 4 * kDqPerQuarter;
-constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantWarps;
-constexpr int kEpilogueWarps = 4 * kEpiPerQuarter;
-// Registers per thread after setmaxnreg: control warpgroup (warps 0-3),
-// dequantisers (4-11), epilogue (12-19).  Their sum over the CTA must not
-// exceed what the launch holds (checked on the host before every launch:
-// a setmaxnreg.inc that cannot be served would wait forever).
-constexpr int kRegCtl = 40, kRegDq = 80, kRegEpi = 120;
-constexpr int kRegBudget = 128 * (kRegCtl + kDqPerQuarter * kRegDq + kEpiPerQuarter * kRegEpi);
-static_assert(kRegBudget <= 65536, "register split exceeds the register file");
+// Warp layouts after the control warpgroup (warps 0-3), both 20 warps:
+//   DQ = 1: one dequantiser and three epilogue warps per TMEM lane quarter
+//           (tiles of many tokens: the accumulator drain sets the stage period)
+//   DQ = 2: two dequantisers and two epilogue warps per quarter (tiles of few
+//           tokens: the fixed per-stage conversion sets it)
+// Registers per thread after setmaxnreg: control, dequantisers, epilogue.  Their
+// sum over the CTA must not exceed what the launch holds (checked on the host
+// before every launch: a setmaxnreg.inc that cannot be served would wait forever).
+template <int DQ>
+struct Layout {
+    static constexpr int kDqPerQuarter = DQ;
+    static constexpr int kEpiPerQuarter = DQ == 1 ? 3 : 2;
+    static constexpr int kDequantWarps = 4 * kDqPerQuarter;
+    static constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantWarps;
+    static constexpr int kEpilogueWarps = 4 * kEpiPerQuarter;
+    static constexpr int kRegCtl = 40, kRegDq = DQ == 1 ? 80 : 56, kRegEpi = DQ == 1 ? 120 : 160;
+    static constexpr int kRegBudget =
+        128 * (kRegCtl + kDqPerQuarter * kRegDq + kEpiPerQuarter * kRegEpi);
+    static_assert(kEpilogueWarp0 + kEpilogueWarps == 20, "20 warps per CTA");
+    static_assert(kRegBudget <= 65536, "register split exceeds the register file");
+};
 constexpr int kStages = 3;                        // shared-memory pipeline depth
 constexpr int kAStagesT = 2;                      // A operand stages in TMEM
 constexpr int kDBufs = 2;                         // accumulator buffers in TMEM
@@ -218,11 +231,16 @@ __device__ __forceinline__ int weight_row(const GroupedParams& p, const TileInfo
 }
 
 // ---------------------------------------------------------------- the kernel
-// G: quantisation group size along K; MODE: kGateUp or kDown (one instantiation
-// each, so each gets its own register allocation).
-template <int G, int MODE>
+// G: quantisation group size along K; MODE: kGateUp or kDown; DQ: the warp layout
+// (Layout).  One instantiation each, so each gets its own register allocation.
+template <int G, int MODE, int DQ>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
+    using L = Layout<DQ>;
+    constexpr int kDqPerQuarter = L::kDqPerQuarter, kEpiPerQuarter = L::kEpiPerQuarter;
+    constexpr int kDequantWarps = L::kDequantWarps, kEpilogueWarp0 = L::kEpilogueWarp0;
+    constexpr int kEpilogueWarps = L::kEpilogueWarps;
+    constexpr int kRegCtl = L::kRegCtl, kRegDq = L::kRegDq, kRegEpi = L::kRegEpi;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -694,26 +712,34 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
     return r == CUDA_SUCCESS;
 }
 
-template <int G, int MODE>
+template <int G, int MODE, int DQ>
 cudaError_t launch_gm(GroupedParams& prm, int sms, cudaStream_t st) {
-    cudaError_t err = ensure_dynamic_smem((const void*)grouped_w4a16_kernel<G, MODE>, kSmemBytes);
+    cudaError_t err = ensure_dynamic_smem((const void*)grouped_w4a16_kernel<G, MODE, DQ>, kSmemBytes);
     if (err != cudaSuccess) return err;
     // the warpgroups' setmaxnreg targets must fit in the registers the launch holds
     static int launch_regs = -1;
     if (launch_regs < 0) {
         cudaFuncAttributes fa;
-        err = cudaFuncGetAttributes(&fa, grouped_w4a16_kernel<G, MODE>);
+        err = cudaFuncGetAttributes(&fa, grouped_w4a16_kernel<G, MODE, DQ>);
         if (err != cudaSuccess) return err;
         launch_regs = fa.numRegs;
     }
-    if (launch_regs * kThreads < kRegBudget) return cudaErrorInvalidConfiguration;
-    grouped_w4a16_kernel<G, MODE><<<sms, kThreads, kSmemBytes, st>>>(prm);
+    if (launch_regs * kThreads < Layout<DQ>::kRegBudget) return cudaErrorInvalidConfiguration;
+    grouped_w4a16_kernel<G, MODE, DQ><<<sms, kThreads, kSmemBytes, st>>>(prm);
     return cudaGetLastError();
 }
 
+// Up to 64 tokens a tile holds at most 64 tokens (kTileN >= 64): the layout with
+// two dequantisers per quarter; above, the one with three epilogue warps.
+constexpr int kSmallTileT = 64;
+
 template <int G>
 cudaError_t launch_g(GroupedParams& prm, int sms, cudaStream_t st) {
-    return prm.mode == kGateUp ? launch_gm<G, kGateUp>(prm, sms, st) : launch_gm<G, kDown>(prm, sms, st);
+    if (prm.T <= kSmallTileT)
+        return prm.mode == kGateUp ? launch_gm<G, kGateUp, 2>(prm, sms, st)
+                                   : launch_gm<G, kDown, 2>(prm, sms, st);
+    return prm.mode == kGateUp ? launch_gm<G, kGateUp, 1>(prm, sms, st)
+                               : launch_gm<G, kDown, 1>(prm, sms, st);
 }
 
 cudaError_t launch(GroupedParams& prm, cudaStream_t st) {
