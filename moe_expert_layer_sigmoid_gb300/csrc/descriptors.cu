@@ -111,8 +111,8 @@ desc_place(const int32_t* __restrict__ topk_idx, int64_t nslots, int E,
 
 constexpr int kScatterThreads = 256;
 
-// Tile schedule of the grouped tcgen05 kernels.  A token tile is up to tn (128,
-// or 256 for the W8A8 kernel) consecutive rows of one group (routed expert or the shared expert); a tile
+// Tile schedule of the grouped tcgen05 kernels.  A token tile is up to tn (192
+// for the W4A16 kernel, 256 for the W8A8 kernel) consecutive rows of one group (routed expert or the shared expert); a tile
 // pairs it with one weight band (gate+up: 64 gate rows and their 64 up rows;
 // down: 128 output channels).  Groups run largest first: the shared expert,
 // then the routed experts in schedule order.  Within a group the order is

@@ -729,8 +729,9 @@ cudaError_t launch_gm(GroupedParams& prm, int sms, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-// Up to 64 tokens a tile holds at most 64 tokens (kTileN >= 64): the layout with
-// two dequantisers per quarter; above, the one with three epilogue warps.
+// A launch of at most 64 tokens has tiles of at most 64 tokens (kTileN >= 64): it
+// takes the layout with two dequantisers per quarter; larger ones the layout
+// with three epilogue warps per quarter.
 constexpr int kSmallTileT = 64;
 
 template <int G>
