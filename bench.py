@@ -130,7 +130,7 @@ def kernels_per_step(cfg, flags=0, fmt="w4"):
     """Kernels libmoe.so launches for one moe_layer_forward (memset nodes excluded)."""
     if fmt == "w8":  # router (2), descriptors (4), x quantiser, GEMM, H quantiser, GEMM, combine
         return 2 + 4 + 1 + 1 + 1 + 1 + 1
-    gemv = (flags & 0x1) or (cfg.T <= 3 and not flags & 0x2)
+    gemv = (flags & 0x1) or (cfg.T <= 2 and not flags & 0x2)
     if gemv and cfg.T == 1 and flags & 0x8:
         return 1  # the cooperative single-launch step
     if gemv and cfg.T <= 64:

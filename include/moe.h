@@ -265,7 +265,7 @@ moe_status_t moe_build_descriptors(const int32_t* topk_idx, const moe_dims_t* di
  *   Wgu_s    shared gate+up, q [2F_s][d/2], s [2F_s][d/group]
  *   H        (device) out: bf16 [T*k + T][max(F, F_s)] (row stride max(F, F_s))
  *   ws       the workspace moe_build_descriptors filled for this batch
- * T <= 3 runs a CUDA-core GEMV, larger T the tcgen05 grouped kernel; the
+ * T <= 2 runs a CUDA-core GEMV, larger T the tcgen05 grouped kernel; the
  * flags can force either (the GEMV needs d <= 4096 and max(F, F_s) <= 2048,
  * the grouped kernel d, F, F_s multiples of 128 and at most 32 quantisation
  * groups per row; a forced path that does not cover the shape returns
@@ -303,7 +303,7 @@ moe_status_t moe_down_w4a16(const uint16_t* H, const moe_dims_t* dims, const int
  *                                           + Y[T*k + t]) ),
  * the same value and summation order as moe_down_w4a16 followed by
  * moe_combine_shared (or moe_combine_shared_residual), without the caller's Y.
- * On the GEMV path (T <= 3 by default) the combine runs inside the down
+ * On the GEMV path (T <= 2 by default) the combine runs inside the down
  * kernel and Y stays in L2; on the grouped path it is the down launch and a
  * combine launch, Y in the workspace.
  *   topk_w   (device) fp32 [T][k], from moe_router_topk
@@ -354,7 +354,7 @@ moe_status_t moe_combine_shared_residual(const float* Y, const float* topk_w, co
  * Same arguments as the calls above; ws must hold moe_layer_workspace_bytes
  * and be zero-filled before its first use (the single-launch decode router
  * keeps a completion counter in it, which every call leaves at zero).
- * On the GEMV path (T <= 3 by default) the call is three launches chained by
+ * On the GEMV path (T <= 2 by default) the call is three launches chained by
  * programmatic dependent launch: the router with the top-k and descriptors in
  * its last CTA, gate+up, and down with the combine fused in; otherwise the
  * router, descriptors, grouped gate+up and down, and combine.

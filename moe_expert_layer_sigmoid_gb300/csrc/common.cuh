@@ -72,11 +72,11 @@ constexpr int kRouterSmallT = 64;
 
 // GEMV (decode) expert path by default for T <= kGemvMaxT, from a sweep of the
 // layer time over T on both forced paths at the decode shapes (GB300): the
-// CUDA-core GEMV took 35.8 / 79 / 110 / 145 us at T = 1 / 2 / 3 / 4 (its
+// CUDA-core GEMV took 35.7 / 77.0 / 107.1 / 141.8 us at T = 1 / 2 / 3 / 4 (its
 // multi-token form is FMA-bound, ~36 us per token), the grouped tensor-core
-// kernel 97 / 104 / 112 / 122 us; the flags can force either.  One pass of the
-// GEMV's loads covers rows of up to kGemvMaxD (gate+up) / kGemvMaxF (down).
-constexpr int kGemvMaxT = 3;
+// kernel 95.6 / 97.7 / 104.8 / 114.5 us; the flags can force either.  One pass of
+// the GEMV's loads covers rows of up to kGemvMaxD (gate+up) / kGemvMaxF (down).
+constexpr int kGemvMaxT = 2;
 constexpr int kGemvMaxD = 4096;
 constexpr int kGemvMaxF = 2048;
 

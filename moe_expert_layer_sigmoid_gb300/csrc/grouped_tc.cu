@@ -40,8 +40,9 @@
 //               registers (packed f32x2 FMAs); at the end of a tile apply
 //               SwiGLU (gate+up) or store Y (down)
 // Launches of at most 64 tokens use the other layout (Layout<2>): warps 4-11
-// dequantise (two per quarter, half of a stage's K each) and warps 12-19 are
-// the epilogue (two per quarter, blocks p, p + 2, p + 4).
+// dequantise (two per quarter, half of a stage's K each), warps 12-19 are the
+// epilogue (two per quarter, 32 columns each), and TMEM holds three 64-column
+// accumulators instead of two 192-column ones.
 //
 // With many tokens per tile the per-group drain of the accumulators is the
 // loop that sets the stage period (MMA -> commit -> epilogue reads ->
@@ -57,9 +58,9 @@
 // Numerics: each group's partial sum is sum_k x_k * q_k with exact bf16
 // products and fp32 accumulation; multiplying by the fp16 scale s in fp32
 // gives sum_k x_k * (q_k * s), the dequantised product, without rounding the
-// weights.  TMEM: two A stages at columns [0, 128), two 192-column
-// accumulators at [128, 512), so the MMAs can run one group ahead of the
-// epilogue.
+// weights.  TMEM: two A stages at columns [0, 128), then two 192-column
+// accumulators (three 64-column ones in the small-tile layout), so the MMAs
+// can run one (two) groups ahead of the epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -74,11 +75,27 @@ namespace {
 constexpr int kWarps = 20;  // control warpgroup + dequantisers + epilogue
 constexpr int kThreads = kWarps * 32;
 constexpr int kDequantWarp0 = 4;
+constexpr int kStages = 3;                        // shared-memory pipeline depth
+constexpr int kAStagesT = 2;                      // A operand stages in TMEM
+constexpr int kMaxDBufs = 3;                      // accumulator buffers in TMEM, at most
+static_assert(kAStagesT < kStages, "dequant reuses the stage barrier of the MMA it waits for");
+constexpr int kKStage = 128;                      // K elements per stage
+constexpr int kTokTile = 192;                     // max tokens (N) per tile
+constexpr int kBStageBytes = 2 * kTokTile * 128;  // two 64-wide K blocks, 128 B per row
+constexpr int kAStageBytes = 128 * 64;            // 128 rows x 64 bytes of nibbles
+constexpr int kMaxGroupsPerRow = 32;              // scale buffer capacity (K / group)
+constexpr int kScBytes = 128 * kMaxGroupsPerRow * 2;
+constexpr int kTmemCols = 512;
+constexpr int kTmemD = kAStagesT * 64;            // first accumulator column
+static_assert(kTokTile == kTileN, "the descriptors' tile lists use kTileN tokens per tile");
+
 // Warp layouts after the control warpgroup (warps 0-3), both 20 warps:
 //   DQ = 1: one dequantiser and three epilogue warps per TMEM lane quarter
 //           (tiles of many tokens: the accumulator drain sets the stage period)
-//   DQ = 2: two dequantisers and two epilogue warps per quarter (tiles of few
-//           tokens: the fixed per-stage conversion sets it)
+//   DQ = 2: two dequantisers and two epilogue warps per quarter and three
+//           64-column accumulators (tiles of at most 64 tokens: the fixed
+//           per-stage conversion and the drain latency set it, and the third
+//           accumulator lets the MMAs run two groups ahead of the drain)
 // Registers per thread after setmaxnreg: control, dequantisers, epilogue.  Their
 // sum over the CTA must not exceed what the launch holds (checked on the host
 // before every launch: a setmaxnreg.inc that cannot be served would wait forever).
@@ -89,40 +106,30 @@ struct Layout {
     static constexpr int kDequantWarps = 4 * kDqPerQuarter;
     static constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantWarps;
     static constexpr int kEpilogueWarps = 4 * kEpiPerQuarter;
+    static constexpr int kDBufs = DQ == 1 ? 2 : 3;          // accumulator buffers in TMEM
+    static constexpr int kAccCols = DQ == 1 ? kTokTile : 64;  // tokens one accumulator holds
     static constexpr int kRegCtl = 40, kRegDq = DQ == 1 ? 80 : 56, kRegEpi = DQ == 1 ? 120 : 160;
     static constexpr int kRegBudget =
         128 * (kRegCtl + kDqPerQuarter * kRegDq + kEpiPerQuarter * kRegEpi);
     static_assert(kEpilogueWarp0 + kEpilogueWarps == 20, "20 warps per CTA");
+    static_assert(kDBufs <= kMaxDBufs, "barrier arrays");
+    static_assert(kTmemD + kDBufs * kAccCols <= 512, "A stages and accumulators exceed the TMEM columns");
     static_assert(kRegBudget <= 65536, "register split exceeds the register file");
 };
-constexpr int kStages = 3;                        // shared-memory pipeline depth
-constexpr int kAStagesT = 2;                      // A operand stages in TMEM
-constexpr int kDBufs = 2;                         // accumulator buffers in TMEM
-static_assert(kAStagesT < kStages, "dequant reuses the stage barrier of the MMA it waits for");
-constexpr int kKStage = 128;                      // K elements per stage
-constexpr int kTokTile = 192;                     // max tokens (N) per tile
-constexpr int kBStageBytes = 2 * kTokTile * 128;  // two 64-wide K blocks, 128 B per row
-constexpr int kAStageBytes = 128 * 64;            // 128 rows x 64 bytes of nibbles
-constexpr int kMaxGroupsPerRow = 32;              // scale buffer capacity (K / group)
-constexpr int kScBytes = 128 * kMaxGroupsPerRow * 2;
-constexpr int kTmemCols = 512;
-constexpr int kTmemD = kAStagesT * 64;            // first accumulator column
-static_assert(kTmemD + kDBufs * kTokTile <= 512, "A stages and accumulators exceed the TMEM columns");
-static_assert(kTokTile == kTileN, "the descriptors' tile lists use kTileN tokens per tile");
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffB = 0;
 constexpr int kOffA = kOffB + kStages * kBStageBytes;
 constexpr int kOffSc = kOffA + kStages * kAStageBytes;
 constexpr int kOffBar = kOffSc + 2 * kScBytes;
-// barriers: FULL[kStages], EMPTY[kStages], AREADY[kAStagesT], DFULL[kDBufs], DEMPTY[kDBufs],
+// barriers: FULL[kStages], EMPTY[kStages], AREADY[kAStagesT], DFULL[kMaxDBufs], DEMPTY[kMaxDBufs],
 // SCFULL[2], SCEMPTY[2]
 // EMPTY[s] completes when the MMAs of smem stage s are done and the dequant
 // warps have read its int4 tile; it also tells the dequant warps that the
 // TMEM A stage those MMAs read is free again.
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAReady = 2 * kStages,
               kBarDFull = kBarAReady + kAStagesT,
-              kBarDEmpty = kBarDFull + kDBufs, kBarScFull = kBarDEmpty + kDBufs,
+              kBarDEmpty = kBarDFull + kMaxDBufs, kBarScFull = kBarDEmpty + kMaxDBufs,
               kBarScEmpty = kBarScFull + 2, kBarTd = kBarScEmpty + 2, kNumBars = kBarTd + 2;
 // TD[2]: one per MMA issuer, committed after an abort so the issuer can wait for
 // its MMAs in flight before the CTA frees TMEM.
@@ -241,6 +248,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
     constexpr int kDequantWarps = L::kDequantWarps, kEpilogueWarp0 = L::kEpilogueWarp0;
     constexpr int kEpilogueWarps = L::kEpilogueWarps;
     constexpr int kRegCtl = L::kRegCtl, kRegDq = L::kRegDq, kRegEpi = L::kRegEpi;
+    constexpr int kDBufs = L::kDBufs, kAccCols = L::kAccCols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -415,7 +423,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t dcol = tmem + (uint32_t)(kTmemD + b * kTokTile);
+                            const uint32_t dcol = tmem + (uint32_t)(kTmemD + b * kAccCols);
     #pragma unroll
                             for (int kk = 0; kk < G / 16; ++kk) {
                                 const int kg = gg * (G / 16) + kk;  // 16-wide K step within the stage
@@ -515,7 +523,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
         // the 32-column blocks part, part + kEpiPerQuarter, ..., so every warp of a
         // quarter has work whenever a tile holds more than 32 * (kEpiPerQuarter - 1)
         // tokens: acc[j] is column col(j)
-        constexpr int kEpiCols = kTokTile / kEpiPerQuarter;
+        constexpr int kEpiCols = kAccCols / kEpiPerQuarter;
         static_assert(kEpiCols % 32 == 0, "whole 32-column blocks per epilogue warp");
         auto col = [&](int j) { return 32 * (kEpiPerQuarter * (j >> 5) + part) + (j & 31); };
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -542,7 +550,7 @@ grouped_w4a16_kernel(const __grid_constant__ GroupedParams p) {
                 if (!ok) continue;
                 tc_fence_after();
                 const float s = __half2float(srow[g]);
-                const uint32_t dcol = tmem + lane_base + (uint32_t)(kTmemD + b * kTokTile);
+                const uint32_t dcol = tmem + lane_base + (uint32_t)(kTmemD + b * kAccCols);
                 // the accumulator is released as soon as the warp's last block of it is
                 // in registers, before that block's FMAs
 #pragma unroll

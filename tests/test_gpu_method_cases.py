@@ -107,8 +107,8 @@ def _layer(C, x, W_r, b, flags, T):
 
 @pytest.mark.parametrize("form", ["t1", "t1_mma", "t3", "t40", "t40_gemv"])
 def test_layer_routes_exact_ties_like_the_oracle(tie_case, form):
-    """The router inside each layer form: the fused decode router (T = 1 and T = 3 on
-    the decode chain, T = 40 forced onto it), the single-launch step's own router, and
+    """The router inside each layer form: the fused decode router (T = 1 on the decode
+    chain, T = 3 and T = 40 forced onto it), the single-launch step's own router, and
     the standalone router before the grouped path (T = 40)."""
     C = tie_case
     cfg = C.cfg
@@ -123,7 +123,7 @@ def test_layer_routes_exact_ties_like_the_oracle(tie_case, form):
         got = np.concatenate([_layer(C, x[t:t + 1], W_r_d, b_d, flags, 1) for t in range(4)])
         want = ref[:4]
     elif form == "t3":
-        got, want = _layer(C, x[:3], W_r_d, b_d, 0, 3), ref[:3]
+        got, want = _layer(C, x[:3], W_r_d, b_d, GEMV, 3), ref[:3]
     else:
         got = _layer(C, x, W_r_d, b_d, GEMV if form == "t40_gemv" else 0, cfg.T)
         want = ref
