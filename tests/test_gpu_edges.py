@@ -31,6 +31,11 @@ EDGE_CONFIGS = [
     (1, 2048, 16, 16, 256, 128, 128),    # k == E at T = 1
     (7, 4096, 32, 10, 1024, 1024, 128),  # decode shapes, several tokens per expert
     (9, 256, 1024, 32, 128, 128, 32),    # the largest E and k the library accepts
+    # grouped-kernel tile and layout boundaries: 64 tokens per expert on the
+    # small-tile layout (64-column accumulators), and 385 tokens per expert on
+    # the 192-token layout (tiles of 192, 192 and 1)
+    (64, 256, 8, 8, 128, 128, 32),
+    (385, 256, 2, 2, 128, 128, 64),
 ]
 
 
