@@ -29,10 +29,11 @@
 // bound by the bytes each SM has in flight over their latency, so 256-token
 // tiles (twice the flops per weight byte of 128-token ones) go faster.
 //
-// Warp roles (6 warps, one CTA per SM): warp 0 TMA producer; warp 1 allocates
-// TMEM and issues the MMAs; warps 2-5 the epilogue (each reads the 32 TMEM
-// lanes of its quarter).  Two 256-column accumulators let the epilogue of one
-// tile overlap the MMAs of the next.
+// Warp roles (10 warps, one CTA per SM): warp 0 TMA producer; warp 1 allocates
+// TMEM and issues the MMAs; warps 2-9 the epilogue, two per TMEM lane quarter
+// (each reads the 32 lanes of its quarter; warps 2-5 take the 32-column chunks
+// 0, 2, 4, ..., warps 6-9 chunks 1, 3, 5, ...).  Two 256-column accumulators
+// let the epilogue of one tile overlap the MMAs of the next.
 #include <cuda.h>
 #include <cuda_fp8.h>
 #include <cudaTypedefs.h>
@@ -43,7 +44,7 @@
 namespace moe {
 namespace {
 
-constexpr int kF8Warps = 6;
+constexpr int kF8Warps = 10;
 constexpr int kF8Threads = kF8Warps * 32;
 constexpr int kF8EpiWarp0 = 2;
 constexpr int kF8Stages = 4;
@@ -258,6 +259,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
         // After a failed wait every epilogue warp keeps walking the tiles
         // (skipping the work), so no warp waits on a barrier the others left.
         const int q = warp & 3;
+        const int half = (warp - kF8EpiWarp0) >> 2;  // which 32-column chunks of a tile
         const int m = q * 32 + lane;  // tile row = TMEM lane
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int gu = (m >> 4) & 1;                     // gate+up: gate (0) or up (1) row
@@ -285,29 +287,37 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                                    : __ldg(p.s_shared + col);
                 }
                 const int npad = (n + 15) & ~15;
-                for (int c0 = 0; c0 < npad; c0 += 32) {
+                for (int c0 = 32 * half; c0 < npad; c0 += 64) {
                     uint32_t v[32];
                     tmem_ld_x32(tmem + lane_base + (uint32_t)(b * kF8Tok + c0), v);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                     const float a_mine = c0 + lane < n ? __ldg(p.a_rows + row0 + c0 + lane) : 0.f;
+                    if (gateup) {
+                        // lane i holds gate row f, lane i ^ 16 the up row of the same f.
+                        // Step j finishes token c0 + j on the gate lanes and c0 + j + 16 on
+                        // the up lanes: each lane sends the value its partner needs
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float aj = __shfl_sync(0xffffffffu, a_mine, j);
-                        const float val = (__uint_as_float(v[j]) * aj) * s_w;
-                        const int nn = c0 + j;
-                        if (gateup) {
-                            // lane i holds gate row f, lane i ^ 16 the up row of the same f;
-                            // gate lanes store tokens j < 16 of the chunk, up lanes the rest
-                            const float other = __shfl_xor_sync(0xffffffffu, val, 16);
-                            const float gv = lo ? val : other;
-                            const float uv = lo ? other : val;
-                            if (lo == (j < 16) && nn < n) {
-                                const float hv = swiglu_f32(gv, uv);
+                        for (int j = 0; j < 16; ++j) {
+                            const float a_lo = __shfl_sync(0xffffffffu, a_mine, j);
+                            const float a_hi = __shfl_sync(0xffffffffu, a_mine, j + 16);
+                            const float v_lo = (__uint_as_float(v[j]) * a_lo) * s_w;
+                            const float v_hi = (__uint_as_float(v[j + 16]) * a_hi) * s_w;
+                            const float other = __shfl_xor_sync(0xffffffffu, lo ? v_hi : v_lo, 16);
+                            const float gv = lo ? v_lo : other;
+                            const float uv = lo ? other : v_hi;
+                            const int nn = c0 + j + (lo ? 0 : 16);
+                            if (nn < n)
                                 reinterpret_cast<uint16_t*>(p.out)[(int64_t)(row0 + nn) * p.ld_out + col] =
-                                    float_to_bf16_bits(hv);
-                            }
-                        } else if (nn < n) {
-                            reinterpret_cast<float*>(p.out)[(int64_t)(row0 + nn) * p.ld_out + col] = val;
+                                    float_to_bf16_bits(swiglu_f32(gv, uv));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float aj = __shfl_sync(0xffffffffu, a_mine, j);
+                            const float val = (__uint_as_float(v[j]) * aj) * s_w;
+                            const int nn = c0 + j;
+                            if (nn < n)
+                                reinterpret_cast<float*>(p.out)[(int64_t)(row0 + nn) * p.ld_out + col] = val;
                         }
                     }
                 }
