@@ -29,11 +29,11 @@
 // bound by the bytes each SM has in flight over their latency, so 256-token
 // tiles (twice the flops per weight byte of 128-token ones) go faster.
 //
-// Warp roles (10 warps, one CTA per SM): warp 0 TMA producer; warp 1 allocates
-// TMEM and issues the MMAs; warps 2-9 the epilogue, two per TMEM lane quarter
-// (each reads the 32 lanes of its quarter; warps 2-5 take the 32-column chunks
-// 0, 2, 4, ..., warps 6-9 chunks 1, 3, 5, ...).  Two 256-column accumulators
-// let the epilogue of one tile overlap the MMAs of the next.
+// Warp roles (14 warps, one CTA per SM): warp 0 TMA producer; warp 1 allocates
+// TMEM and issues the MMAs; warps 2-13 the epilogue, three per TMEM lane quarter
+// (each reads the 32 lanes of its quarter; the warp of part p takes the
+// 32-column chunks p, p + 3, ...).  Two 256-column accumulators let the
+// epilogue of one tile overlap the MMAs of the next.
 #include <cuda.h>
 #include <cuda_fp8.h>
 #include <cudaTypedefs.h>
@@ -44,7 +44,8 @@
 namespace moe {
 namespace {
 
-constexpr int kF8Warps = 10;
+constexpr int kF8Warps = 14;
+constexpr int kF8EpiPerQuarter = (kF8Warps - 2) / 4;
 constexpr int kF8Threads = kF8Warps * 32;
 constexpr int kF8EpiWarp0 = 2;
 constexpr int kF8Stages = 4;
@@ -259,7 +260,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
         // After a failed wait every epilogue warp keeps walking the tiles
         // (skipping the work), so no warp waits on a barrier the others left.
         const int q = warp & 3;
-        const int half = (warp - kF8EpiWarp0) >> 2;  // which 32-column chunks of a tile
+        const int part = (warp - kF8EpiWarp0) >> 2;  // which 32-column chunks of a tile
         const int m = q * 32 + lane;  // tile row = TMEM lane
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int gu = (m >> 4) & 1;                     // gate+up: gate (0) or up (1) row
@@ -287,7 +288,7 @@ grouped_w8a8_kernel(const __grid_constant__ F8Params p) {
                                    : __ldg(p.s_shared + col);
                 }
                 const int npad = (n + 15) & ~15;
-                for (int c0 = 32 * half; c0 < npad; c0 += 64) {
+                for (int c0 = 32 * part; c0 < npad; c0 += 32 * kF8EpiPerQuarter) {
                     uint32_t v[32];
                     tmem_ld_x32(tmem + lane_base + (uint32_t)(b * kF8Tok + c0), v);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
