@@ -138,12 +138,27 @@ __device__ __forceinline__ void router_topk_warp(const float* partial, int kspli
                                                  int32_t* __restrict__ topk_idx,
                                                  float* __restrict__ topk_w,
                                                  float* __restrict__ margin, int* sel_e) {
-    float key[NV], sv[NV];
+    float key[NV], sv[NV], lg[NV];
+    // the lane's NV logits, each summed over its partials in kc order (as
+    // router_logit); one round of NV independent loads per partial, so the
+    // loads of all NV experts are in flight together
+#pragma unroll
+    for (int i = 0; i < NV; ++i) lg[i] = 0.f;
+    {
+        const float* p = partial + (int64_t)t * E + lane;
+        const int64_t step = (int64_t)T * E;
+#pragma unroll 2
+        for (int kc = 0; kc < ksplit; ++kc) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                if (lane + 32 * i < E) lg[i] += __ldcg(p + kc * step + 32 * i);
+        }
+    }
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
         if (e < E) {
-            const float l = router_logit(partial, ksplit, T, E, t, e);
+            const float l = lg[i];
             const float s = 1.0f / (1.0f + expf(-l));
             sv[i] = s;
             key[i] = s + __ldg(bias + e);
