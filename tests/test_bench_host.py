@@ -1,6 +1,7 @@
 """bench.py's contract on the host (no GPU): the reference arm's JSON line, argument checks,
 the launch count per step, and the replicas' max-over-ranks step time over a two-rank gloo
 group."""
+import dataclasses
 import json
 import os
 import socket
@@ -84,6 +85,13 @@ def test_reference_config_is_the_gpu_arms_config():
                                           ("decode1", 2, 10), ("decode1", 8, 1)])
 def test_kernels_per_step(name, flags, n):
     assert bench.kernels_per_step(workloads.CONFIGS[name], flags) == n
+
+
+@pytest.mark.parametrize("T,n", [(1, 3), (2, 3), (3, 10), (64, 10)])
+def test_kernels_per_step_follows_the_crossover(T, n):
+    """The GEMV chain (three launches) up to T = 2, the grouped path from T = 3."""
+    cfg = dataclasses.replace(workloads.CONFIGS["decode1"], T=T)
+    assert bench.kernels_per_step(cfg, 0) == n
 
 
 def _free_port():
