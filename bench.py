@@ -27,6 +27,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -688,12 +689,29 @@ def run_reference(args):
         "steps_timed": n,
         "cpu_baseline": {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{n} tokens of {cfg.name}, one per step, single thread "
-                                   f"(at most {REF_BUDGET_S:.0f} s of oracle work)"},
+                                   f"(at most {REF_BUDGET_S:.0f} s of oracle work)",
+                         **host_cpu()},
         "e2e": {"value": round(tps, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def host_cpu():
+    """The host the oracle ran on: processor name (best effort) and its core count."""
+    name = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "hardware", "cpu part") and ":" in ln:
+                    name = ln.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    return {"cpu": name or platform.processor() or platform.machine(), "nproc": os.cpu_count()}
 
 
 def main():
@@ -766,7 +784,7 @@ def main():
         n, sec = oracle_sample(cfg, args.cpu_budget, 10 ** 6)
         cpu = {"value": round(n / sec, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} single tokens of {cfg.name} (router + {cfg.k} experts + shared), "
-                         f"{sec:.1f} s of single-thread CPU work"}
+                         f"{sec:.1f} s of single-thread CPU work", **host_cpu()}
 
     if rank == 0:
         roof = (roofline_of(main_res, ms, pk, pk_kind) if args.fmt == "w4" else
