@@ -10,18 +10,18 @@
 //
 // Shape of one tile: M = 128 weight rows (swap-AB: weights take the M slot),
 // N = up to 192 tokens of one expert (rounded up to 16), K = the full
-// contraction in stages of 128.  192 is the widest N for which two A stages and
-// two accumulators fit in the 512 TMEM columns; against 128-token tiles it cuts
-// the MMA instructions per flop by a third, and the dequantisation passes over
-// each weight tile (one per token tile) by up to a third.  A gate+up tile holds 64 gate rows and the 64
-// matching up rows, interleaved in blocks of 16 (gate f..f+15, up f..f+15,
-// ...), so a gate row and its up row sit 16 lanes apart in the same warp and
-// SwiGLU is finished with one shuffle.
+// contraction in stages of 128.  192 is the widest N for which two A stages and two
+// accumulators fit in the 512 TMEM columns; against 128-token tiles it cuts the
+// MMA instructions per flop by a third, and the dequantisation passes over each
+// weight tile (one per token tile) by up to a third.  A gate+up tile holds 64
+// gate rows and the 64 matching up rows, interleaved in blocks of 16 (gate
+// f..f+15, up f..f+15, ...), so a gate row and its up row sit 16 lanes apart in
+// the same warp and SwiGLU is finished with one shuffle.
 //
-// Activation rows are read as plain TMA boxes of up to 192 rows: the down projection
-// reads H, whose rows are already grouped by expert; gate+up reads x gathered
-// once into that same row order (gather_rows_kernel), which replaces per-row
-// gathers inside the GEMM that the TMA unit serves slowly.
+// Activation rows are read as plain TMA boxes of up to 192 rows: the down
+// projection reads H, whose rows are already grouped by expert; gate+up reads x
+// gathered once into that same row order (gather_rows_kernel), which replaces
+// per-row gathers inside the GEMM that the TMA unit serves slowly.
 //
 // Warp roles (20 warps, one CTA per SM; setmaxnreg moves registers from the
 // control and dequantiser warpgroups to the epilogue's):
@@ -44,16 +44,16 @@
 // epilogue (two per quarter, 32 columns each), and TMEM holds three 64-column
 // accumulators instead of two 192-column ones.
 //
-// With many tokens per tile the per-group drain of the accumulators is the
-// loop that sets the stage period (MMA -> commit -> epilogue reads ->
-// accumulator free -> next MMA), so the epilogue gets three warps per quarter
-// (two TMEM round trips per group and warp instead of three) and the
-// dequantisers, which convert before they wait for their TMEM slot, one.  With
-// few tokens the conversion, paid per stage whatever the token count, sets it.  Two MMA issuers on two schedulers hide each
-// other's barrier and commit latency; each TMEM A slot is used by every second
-// stage, so splitting the stages by parity gives every AREADY barrier a single
-// waiter that consumes its phases in order (a parity wait cannot tell phase k
-// from phase k - 2).
+// With many tokens per tile the per-group drain of the accumulators is the loop
+// that sets the stage period (MMA -> commit -> epilogue reads -> accumulator
+// free -> next MMA), so the epilogue gets three warps per quarter (two TMEM
+// round trips per group and warp instead of three) and the dequantisers, which
+// convert before they wait for their TMEM slot, one.  With few tokens the
+// conversion, paid per stage whatever the token count, sets it.  Two MMA
+// issuers on two schedulers hide each other's barrier and commit latency; each
+// TMEM A slot is used by every second stage, so splitting the stages by parity
+// gives every AREADY barrier a single waiter that consumes its phases in order
+// (a parity wait cannot tell phase k from phase k - 2).
 //
 // Numerics: each group's partial sum is sum_k x_k * q_k with exact bf16
 // products and fp32 accumulation; multiplying by the fp16 scale s in fp32
